@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV attention hot path on one GB300 (or N, as independent replicas).
+
+One step = one decode step of the memory-bound workload: 64 sequences x 4096 cached tokens,
+32 query / 8 KV heads, head_dim 128, block 16, bf16 (1,073,741,824 bytes of K+V):
+  1. pa_reshape_and_cache writes the step's 64 new key/value rows into the pools;
+  2. pa_paged_attention_decode (split-KV kernel + log-sum-exp combine) answers the 64 queries.
+The headline value is decode HBM throughput: algorithmic bytes (the K/V of every cached
+position read once, q, out, the used block-table entries, the new rows) per second.
+A second leg times causal prefill of 4 x 8192 tokens (block 64): the prompt's cache write
+plus pa_paged_attention_varlen, reported in TFLOP/s of causal attention.
+
+The inputs (1.07 GB of cache per step, 0.4 GB for prefill) exceed the 129 MB L2, so no
+flush is needed between timed steps.
+
+--impl reference times the float64 CPU oracle (the only reference this method has) on a
+bounded sample of the same workload and prints the same metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn HBM GB/s (% of peak) at 64x4096; prefill TFLOP/s"
+DECODE_WORKLOAD = "decode_64x4096_bf16"
+PREFILL_WORKLOAD = "prefill_4x8192_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- accounting
+def kv_bytes_per_token(num_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    """Bytes of one cached position of one layer: a key and a value row per KV head."""
+    return 2 * num_kv_heads * head_dim * elem_bytes
+
+
+def decode_call_bytes(context_lens, num_q_heads, num_kv_heads, head_dim, block_size, elem_bytes) -> int:
+    """Algorithmic bytes of one decode call: every cached position's K and V once, the
+    queries, the outputs, the used block-table entries and the lengths."""
+    kv = sum(int(L) for L in context_lens) * kv_bytes_per_token(num_kv_heads, head_dim, elem_bytes)
+    S = len(context_lens)
+    qo = 2 * S * num_q_heads * head_dim * elem_bytes
+    tables = sum(-(-int(L) // block_size) for L in context_lens) * 4 + S * 4
+    return kv + qo + tables
+
+
+def cache_write_bytes(num_tokens, num_kv_heads, head_dim, elem_bytes) -> int:
+    """reshape_and_cache: read and write each new key and value row, read the slot."""
+    return 2 * num_tokens * kv_bytes_per_token(num_kv_heads, head_dim, elem_bytes) + 4 * num_tokens
+
+
+def causal_flops(q_lens, seq_lens, num_q_heads, head_dim, causal=True) -> float:
+    """4 * D flops (q.k and p.v) per visible (query, key) pair per query head."""
+    pairs = 0
+    for ql, L in zip(q_lens, seq_lens):
+        ql, L = int(ql), int(L)
+        if causal:
+            prior = L - ql
+            pairs += ql * prior + ql * (ql + 1) // 2
+        else:
+            pairs += ql * L
+    return 4.0 * head_dim * num_q_heads * pairs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of the dominant kernels from the committed ncu summary, when the
+    kernels have not changed since (the summary records the source hash it was taken at)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if d.get("source_hash") != source_hash():
+        return {}
+    return d.get("per_launch_bytes", {})
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = set()
+        for r in rows:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    seen.add(n)
+        loaded = [r for r in rows if r[2] > 250.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": sorted(seen), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def time_oracle_decode(case, ko, vo, budget_s: float = 12.0, max_seqs: int | None = None):
+    """Time the float64 oracle on whole sequences of the decode workload, as many as fit
+    ~budget_s (at least one). Returns (GB/s of algorithmic bytes, seconds, seqs, threads)."""
+    import oracle
+    S = case.num_reqs
+    lens = case.seq_lens.tolist()
+    t0 = time.perf_counter()
+    oracle.paged_attention_decode(case.q, ko, vo, case.block_tables, case.seq_lens, case.scale, seqs=[0])
+    one = max(time.perf_counter() - t0, 1e-3)
+    n = max(1, min(S if max_seqs is None else max_seqs, int(budget_s / one)))
+    seqs = list(range(n))
+    t0 = time.perf_counter()
+    oracle.paged_attention_decode(case.q, ko, vo, case.block_tables, case.seq_lens, case.scale, seqs=seqs)
+    dt = time.perf_counter() - t0
+    nbytes = decode_call_bytes([lens[s] for s in seqs], case.num_q_heads, case.num_kv_heads, case.head_dim,
+                               case.block_size, case.q.element_size())
+    return nbytes / dt / 1e9, dt, n, torch.get_num_threads()
+
+
+def oracle_pools(case):
+    import oracle
+    kc, vc = case.empty_pools()
+    oracle.reshape_and_cache(case.key, case.value, kc, vc, case.slot_mapping)
+    return kc, vc
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the float64 CPU oracle, timed as it stands on the host cores, on
+    bounded samples of the decode workload (rank 0 only)."""
+    if rank != 0:
+        return
+    import workloads
+    case = workloads.NAMED[DECODE_WORKLOAD]()
+    ko, vo = oracle_pools(case)
+    import oracle
+    lens = case.seq_lens.tolist()
+    per_step = 2  # sequences per timed step: a bounded sample of the 64
+    seqs_of = lambda i: [(i * per_step + j) % case.num_reqs for j in range(per_step)]  # noqa: E731
+    for i in range(args.warmup):
+        oracle.paged_attention_decode(case.q, ko, vo, case.block_tables, case.seq_lens, case.scale, seqs=seqs_of(i))
+    total_bytes, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        s = seqs_of(args.warmup + i)
+        oracle.paged_attention_decode(case.q, ko, vo, case.block_tables, case.seq_lens, case.scale, seqs=s)
+        total_bytes += decode_call_bytes([lens[j] for j in s], case.num_q_heads, case.num_kv_heads, case.head_dim,
+                                         case.block_size, 2)
+    dt = time.perf_counter() - t0
+    value = total_bytes / dt / 1e9
+    sample = f"{per_step} of 64 sequences per step (all heads, full 4096-token contexts)"
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DECODE_WORKLOAD, "num_seqs": 64, "context_len": 4096, "num_q_heads": 32,
+                       "num_kv_heads": 8, "head_dim": 128, "block_size": 16, "sample": sample},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": torch.get_num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU legs
+def decode_leg(args, world, rank, dev):
+    import paged_kv_attention_gb300 as pa
+    import workloads
+    case = workloads.NAMED[DECODE_WORKLOAD]()
+    S, Hq, Hkv, D, bs = case.num_reqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
+    lens = case.seq_lens.tolist()
+    kc, vc = (t.to(dev) for t in case.empty_pools())
+    pa.reshape_and_cache(case.key.to(dev), case.value.to(dev), kc, vc, case.slot_mapping.to(dev))
+    # the step's new rows: the last cached position of every sequence
+    offs = torch.cumsum(case.seq_lens.long(), 0) - 1
+    new_k, new_v = case.key[offs].contiguous(), case.value[offs].contiguous()
+    new_slots = case.slot_mapping[offs].contiguous()
+    q = case.q.to(dev)
+    tables = case.block_tables.to(dev)
+    ctx = case.seq_lens.to(dev)
+    nk, nv, ns = new_k.to(dev), new_v.to(dev), new_slots.to(dev)
+    out = torch.empty_like(q)
+    splits = pa.decode_auto_splits(S, Hq, Hkv, D, bs, tables.shape[1], case.dtype)
+    ws = torch.empty(max(pa.decode_workspace_bytes(S, Hq, D, tables.shape[1], bs, splits), 16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(qd, kd, vd, sd, ld, od):
+        pa.reshape_and_cache(kd, vd, kc, vc, sd)
+        pa.paged_attention_decode(qd, kc, vc, tables, ld, case.scale, num_splits=splits, out=od, workspace=ws)
+
+    for _ in range(args.warmup):
+        step(q, nk, nv, ns, ctx, out)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        pa.reshape_and_cache(nk, nv, kc, vc, ns)
+        ev[i][1].record(stream)
+        pa.paged_attention_decode(q, kc, vc, tables, ctx, case.scale, num_splits=splits, out=out, workspace=ws)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world)
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    call_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+
+    call_bytes = decode_call_bytes(lens, Hq, Hkv, D, bs, 2)
+    step_bytes = call_bytes + cache_write_bytes(S, Hkv, D, 2)
+    value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
+
+    # end to end: host buffers in, host result out, inside the timed region
+    hq = q.cpu().pin_memory()
+    hk, hv, hs, hl = (t.pin_memory() for t in (new_k, new_v, new_slots, case.seq_lens))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    for _ in range(max(3, args.warmup // 4)):
+        step(q, nk, nv, ns, ctx, out)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_start = torch.cuda.Event(enable_timing=True)
+    e2e_end = torch.cuda.Event(enable_timing=True)
+    e2e_start.record(stream)
+    for i in range(args.steps):
+        q.copy_(hq, non_blocking=True)
+        nk.copy_(hk, non_blocking=True)
+        nv.copy_(hv, non_blocking=True)
+        ns.copy_(hs, non_blocking=True)
+        ctx.copy_(hl, non_blocking=True)
+        step(q, nk, nv, ns, ctx, out)
+        hout.copy_(out, non_blocking=True)
+    e2e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end), world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl))
+    d2h = hout.numel() * hout.element_size()
+    e2e_value = world * step_bytes * args.steps / (e2e_ms / 1e3) / 1e9
+    return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
+                call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=e2e_value, h2d=h2d, d2h=d2h,
+                launches=args.steps * (2 + (1 if splits > 1 else 0)))
+
+
+def prefill_leg(args, dev, steps):
+    import paged_kv_attention_gb300 as pa
+    import workloads
+    case = workloads.NAMED[PREFILL_WORKLOAD]()
+    kc, vc = (t.to(dev) for t in case.empty_pools())
+    q = case.q.to(dev)
+    key, value, slots = case.key.to(dev), case.value.to(dev), case.slot_mapping.to(dev)
+    qsl, sl, tables = case.query_start_loc.to(dev), case.seq_lens.to(dev), case.block_tables.to(dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa.reshape_and_cache(key, value, kc, vc, slots)
+        pa.paged_attention_varlen(q, kc, vc, qsl, sl, tables, case.max_query_len, True, case.scale, out=out)
+
+    for _ in range(max(2, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        pa.reshape_and_cache(key, value, kc, vc, slots)
+        ev[i][1].record(stream)
+        pa.paged_attention_varlen(q, kc, vc, qsl, sl, tables, case.max_query_len, True, case.scale, out=out)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    ql = (case.query_start_loc[1:] - case.query_start_loc[:-1]).tolist()
+    flops = causal_flops(ql, case.seq_lens.tolist(), case.num_q_heads, case.head_dim)
+    return dict(case=case, write_ms=write_ms, attn_ms=attn_ms, flops=flops, tflops=flops / (attn_ms / 1e3) / 1e12,
+                launches=2 * steps)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+    traffic = load_traffic()
+
+    with ClockSampler(local) as clocks:
+        d = decode_leg(args, world, rank, dev)
+        p = None if args.no_prefill else prefill_leg(args, dev, args.prefill_steps)
+    clk = clocks.summary()
+
+    case = d["case"]
+    dec_achieved = d["call_bytes"] / (d["call_ms"] / 1e3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    line = {
+        "metric": METRIC,
+        "value": round(d["value"], 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(d["total_ms"] / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "num_seqs": case.num_reqs, "context_len": 4096,
+                   "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+                   "block_size": case.block_size, "num_splits": d["splits"],
+                   "step": "reshape_and_cache(64 new rows) + decode(split-KV + combine)",
+                   "l2": "no flush: 1.07 GB of K/V per step > 129 MB L2",
+                   "parallelism": "replicas" if world == 1 else f"dp{world} (independent batches per GPU)"},
+        "hbm_frac_of_peak": round(d["value"] / world / hbm, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode call (decode_bf16_kernel + combine_kernel)",
+                     "achieved": round(dec_achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(dec_achieved / hbm, 4), "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": d["call_bytes"], "launch_ms": round(d["call_ms"], 5),
+                     "traffic": traffic.get("decode_bf16_kernel")},
+        "cache_write_ms": round(d["write_ms"], 5),
+        "e2e": {"value": round(d["e2e_value"], 2), "unit": "GB/s", "h2d_bytes_per_step": d["h2d"],
+                "d2h_bytes_per_step": d["d2h"]},
+        "gpu_launches": d["launches"],
+        "clocks": clk,
+    }
+    if p is not None:
+        tf_peak = peaks["bf16_tflops"]
+        line["prefill"] = {
+            "workload": PREFILL_WORKLOAD, "value": round(p["tflops"], 2), "unit": "TFLOP/s",
+            "attn_ms": round(p["attn_ms"], 4), "cache_write_ms": round(p["write_ms"], 4),
+            "causal_flops": p["flops"], "steps": args.prefill_steps, "gpu_launches": p["launches"],
+            "roofline": {"bound": "tensor", "kernel": "varlen attention", "achieved": round(p["tflops"], 2),
+                         "peak": tf_peak, "unit": "TFLOP/s", "frac": round(p["tflops"] / tf_peak, 4),
+                         "peak_source": peak_src, "traffic": traffic.get("varlen_kernel")},
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        _, ko_vo = None, oracle_pools(case)
+        v, dt, n, threads = time_oracle_decode(case, *ko_vo)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} of 64 sequences (full 4096-token contexts, all 32 heads), "
+                                          f"{dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

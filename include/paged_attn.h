@@ -1,0 +1,169 @@
+/*
+ * paged_attn.h - C ABI of the GB300 (sm_103a) paged KV attention library.
+ *
+ * FlashAttention-style attention over a block-paged KV cache with grouped-query
+ * heads: a cache write, a split-KV decode (partials + log-sum-exp combine) and a
+ * causal varlen kernel for prefill, speculative verify and mixed batches.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller. The library never
+ *   allocates, frees or synchronises inside a call; work is enqueued on `stream`
+ *   (a cudaStream_t passed as void*; NULL = the legacy default stream). Calls are
+ *   therefore legal inside CUDA-graph capture.
+ * - Layouts are dense row-major (last index fastest):
+ *     q, out          [N, Hq, D]                 (N = sequences for decode, tokens for varlen)
+ *     k_cache/v_cache [num_blocks, block_size, Hkv, D]
+ *     block_tables    [R, max_blocks_per_seq] int32, a row's unused tail may hold any page id
+ *     key/value       [num_tokens, Hkv, D]
+ *   Every tensor pointer must be 16-byte aligned.
+ * - dtype: PA_DTYPE_BF16 (bf16 storage, fp32 scores/softmax/accumulation, probabilities
+ *   rounded to bf16 for the P.V product) or PA_DTYPE_F32 (fp32 throughout, no TF32).
+ * - Positions come from device buffers (lengths, query_start_loc), never from launch
+ *   arguments, so a captured graph stays valid as sequences grow. Launch shapes depend
+ *   only on the host integers of each call.
+ * - Shape and scalar errors are refused on the host before anything is enqueued.
+ *   Data errors that only the device can see (a page id outside the pool, a length
+ *   beyond the table, a slot outside the pool, a query block longer than its
+ *   sequence) are clamped or skipped so that no kernel reads or writes out of bounds;
+ *   if `error_word` is non-NULL (a device int32 the caller zeroes) the kernel ORs a
+ *   PA_ERRBIT_* bit into it. No kernel traps or asserts.
+ *
+ * Sources of the operations (by page title and section):
+ *   "32. Production attention kernels": One kernel for the whole batch (unified varlen
+ *     kernel, GQA packing, positions from lengths); Long contexts: split the keys
+ *     (split-KV partials, log-sum-exp merge, split-count heuristic); Quantized KV
+ *     caches (write through slot_mapping).
+ *   "TileInfer.jl - Attention kernels": Walking the block table; Decode: GQA packing and
+ *     split-KV (unnormalised fp32 partials, neutral partials for empty splits).
+ *   "poot - Attention and KV Cache": Split-KV decode ((o, m, l) partials, combine);
+ *     KV cache (write map, -1 = padding token writes nothing).
+ *   "paged-attn-xpu": Usage (paged_attention_decode argument list, scale default),
+ *     Validation (empty context gives zeros).
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, Hq % Hkv != 0, misalignment */
+  PA_ERR_UNSUPPORTED = 2,        /* a shape or dtype this build has no kernel for           */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3,
+  PA_ERR_CUDA = 4                /* a CUDA runtime/driver call failed (launch, tensor map)  */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_DTYPE_F32 = 0,
+  PA_DTYPE_BF16 = 1
+} pa_dtype;
+
+/* Bits a kernel ORs into *error_word (see conventions above). */
+#define PA_ERRBIT_PAGE_OUT_OF_POOL   1  /* table entry outside [0, num_blocks): that page reads as zeros   */
+#define PA_ERRBIT_LENGTH_OUT_OF_RANGE 2 /* length < 0 or > max_blocks_per_seq*block_size: clamped          */
+#define PA_ERRBIT_SLOT_OUT_OF_POOL   4  /* slot >= num_blocks*block_size or < -1: token not written         */
+#define PA_ERRBIT_QUERY_LAYOUT       8  /* query_start_loc not monotone or q_len > seq_len: rows zeroed     */
+#define PA_ERRBIT_WAIT_TIMEOUT      16  /* an internal bounded wait expired: that tile's output is invalid */
+
+/* Human-readable name of a status code. Never NULL. */
+const char* pa_status_string(int status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int pa_version(void);
+
+/* Supported-shape query: 1 if the decode (is_varlen=0) or varlen (is_varlen=1) entry point
+ * has a kernel for this head_dim / group / block_size / dtype, else 0. Host only. */
+int pa_supports(int is_varlen, int head_dim, int num_q_heads, int num_kv_heads,
+                int block_size, pa_dtype dtype);
+
+/* Split-count heuristic of the decode path (host only, no CUDA call).
+ * Source: "32. Production attention kernels", Long contexts: split the keys (choose_splits:
+ * enough programs to fill the GPU, no split smaller than a few blocks, at most 32), taken
+ * further here: among the admissible counts, the one whose CTA count best fills whole waves
+ * of `num_sms * ctas_per_sm` resident CTAs.
+ *   num_units        = num_seqs * num_kv_heads (CTAs per split)
+ *   max_chunks       = cdiv(max_blocks_per_seq * block_size, 16) (16-token chunks per row)
+ * Returns a count in [1, 32]; 1 for degenerate inputs. */
+int pa_plan_decode_splits(int num_units, int max_chunks, int num_sms, int ctas_per_sm);
+
+/* The split count an auto (num_splits = 0) pa_paged_attention_decode call with these sizes
+ * uses on the CURRENT device (queries the SM count and the kernel's occupancy once per
+ * device). Returns 0 for arguments the decode call would refuse. */
+int pa_decode_auto_splits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int max_blocks_per_seq, pa_dtype dtype);
+
+/* Bytes of fp32 workspace pa_paged_attention_decode needs for these sizes and `num_splits`
+ * (0 = auto: the bound for any count the heuristic can pick). Host only. Layout inside:
+ * partial accumulators [S, splits, Hq, D] then (m, l) pairs [S, splits, Hq, 2]. 0 when
+ * one split suffices for every choice (then workspace may be NULL). */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int num_splits);
+
+/* reshape_and_cache: for each token i with slot = slot_mapping[i] >= 0, copy key[i] to
+ * k_cache[slot / block_size, slot % block_size] and value[i] likewise (bit-exact copy);
+ * slot -1 writes nothing. Sources: "poot - Attention and KV Cache", KV cache (write map);
+ * "32. Production attention kernels", Quantized KV caches (write_kv via slot_mapping).
+ * key, value: [num_tokens, Hkv, D]; k_cache, v_cache: [num_blocks, block_size, Hkv, D];
+ * slot_mapping: [num_tokens] int32. Two tokens naming one slot is the caller's error (the
+ * result is one of them). A slot outside the pool is skipped and flagged. */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               void* k_cache, void* v_cache,
+                               const int32_t* slot_mapping, int num_tokens,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               pa_dtype dtype, int32_t* error_word, void* stream);
+
+/* paged_attention_decode: one query per sequence, split-KV.
+ * out[s, h] = softmax_p(scale * q[s,h] . K[s,p]) . V[s,p] over p in [0, context_lens[s]),
+ * where K[s,p] = k_cache[block_tables[s, p / block_size], p % block_size, h / (Hq/Hkv)].
+ * context_lens include the query's own (already cached) position; a zero length gives a
+ * zero row. Sources: "paged-attn-xpu", Usage and Method; "TileInfer.jl - Attention
+ * kernels", Decode: GQA packing and split-KV; "32. Production attention kernels", Long
+ * contexts: split the keys.
+ *   q [S, Hq, D], out [S, Hq, D] (dtype); block_tables [S, max_blocks_per_seq] int32;
+ *   context_lens [S] int32; scale: 0 = 1/sqrt(D); num_splits: 0 = auto (heuristic above),
+ *   else 1..32. workspace: device fp32 scratch of >= pa_decode_workspace_bytes(...) bytes
+ *   (may be NULL when that is 0); it is fully overwritten, needs no initialisation, and must
+ *   not be shared by calls that overlap on the GPU.
+ * Supported: D in {64, 128, 256}; bf16 with Hq/Hkv <= 16 and block_size % 16 == 0;
+ *   f32 with (Hq/Hkv) * D <= 2048 and any block_size >= 1. */
+pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int num_blocks, int max_blocks_per_seq,
+                                    float scale, pa_dtype dtype, int num_splits,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    int32_t* error_word, void* stream);
+
+/* paged_attention_varlen: a flattened batch of R requests (prefill chunks, decodes and
+ * verify blocks mixed). Request r owns query rows [query_start_loc[r], query_start_loc[r+1])
+ * of q; its q_len queries are the newest q_len of its seq_lens[r] cached positions (query
+ * t sits at position seq_lens[r] - q_len + t) and, when causal != 0, see keys at positions
+ * <= their own; otherwise all seq_lens[r] keys. A query with no visible key gives zeros.
+ * Sources: "32. Production attention kernels", One kernel for the whole batch;
+ * "TileInfer.jl - Attention kernels", Prefill and Walking the block table.
+ *   q, out [num_tokens, Hq, D]; query_start_loc [R+1] int32 (query_start_loc[R] must equal
+ *   num_tokens); seq_lens [R] int32; block_tables [R, max_blocks_per_seq] int32;
+ *   max_query_len: host upper bound on any q_len (fixes the grid; longer blocks are flagged
+ *   and their excess rows left unwritten... see PA_ERRBIT_QUERY_LAYOUT).
+ * Supported: D in {64, 128, 256}; bf16 with Hq/Hkv in {1,2,4,8,16} (tensor-core path for
+ *   D = 128 and block_size % 16 == 0), f32 with (Hq/Hkv) * D <= 2048. */
+pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* query_start_loc, const int32_t* seq_lens,
+                                    const int32_t* block_tables,
+                                    int num_reqs, int num_tokens, int max_query_len,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int num_blocks, int max_blocks_per_seq,
+                                    int causal, float scale, pa_dtype dtype,
+                                    void* out, int32_t* error_word, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* PAGED_ATTN_H_ */

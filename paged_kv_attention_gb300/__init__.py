@@ -1,0 +1,153 @@
+"""Paged KV attention for GB300 (sm_103a): a thin Python binding over libpagedattn.so.
+
+The functions below only marshal torch tensors into the C ABI of
+``include/paged_attn.h`` (pointers, sizes, the current CUDA stream) and turn a
+non-OK status into an exception. Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and calling any of
+them without the built library raises.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "PagedAttentionError",
+    "decode_auto_splits",
+    "decode_workspace_bytes",
+    "plan_decode_splits",
+    "paged_attention_decode",
+    "paged_attention_varlen",
+    "reshape_and_cache",
+    "status_string",
+    "supports",
+]
+
+_DTYPES = {torch.bfloat16: _lib.PA_DTYPE_BF16, torch.float32: _lib.PA_DTYPE_F32}
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {status_string(status)}")
+        self.status = status
+
+
+def status_string(status: int) -> str:
+    return _lib.load().pa_status_string(int(status)).decode()
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise PagedAttentionError("dtype", _lib.PA_ERR_UNSUPPORTED) from None
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the C ABI must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(fn: str, status: int) -> None:
+    if status != _lib.PA_OK:
+        raise PagedAttentionError(fn, status)
+
+
+def supports(is_varlen: bool, head_dim: int, num_q_heads: int, num_kv_heads: int, block_size: int,
+             dtype: torch.dtype) -> bool:
+    return bool(_lib.load().pa_supports(int(is_varlen), head_dim, num_q_heads, num_kv_heads, block_size,
+                                        _DTYPES.get(dtype, -1)))
+
+
+def plan_decode_splits(num_units: int, max_chunks: int, num_sms: int, ctas_per_sm: int) -> int:
+    return _lib.load().pa_plan_decode_splits(num_units, max_chunks, num_sms, ctas_per_sm)
+
+
+def decode_auto_splits(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                       max_blocks_per_seq: int, dtype: torch.dtype) -> int:
+    """Split count an auto decode call with these sizes uses on the current device (0 = refused)."""
+    return _lib.load().pa_decode_auto_splits(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                             max_blocks_per_seq, _DTYPES.get(dtype, -1))
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_blocks_per_seq: int,
+                           block_size: int, num_splits: int = 0) -> int:
+    return int(_lib.load().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
+                                                     block_size, num_splits))
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, error_word: torch.Tensor | None = None,
+                      stream: torch.cuda.Stream | None = None) -> None:
+    """k_cache[slot // bs, slot % bs] = key[i] for slot = slot_mapping[i] >= 0 (same for v)."""
+    n, hkv, d = key.shape
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
+    st = _lib.load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(slot_mapping), n, hkv, d, bs, nb, _dtype(key),
+                                          _ptr(error_word), _stream(stream))
+    _check("pa_reshape_and_cache", st)
+
+
+def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           scale: float | None = None, num_splits: int = 0,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           error_word: torch.Tensor | None = None,
+                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """One query per sequence over its paged context (split-KV + combine in the library).
+
+    ``workspace`` (a byte or fp32 CUDA tensor) is allocated here when not given; pass one
+    to keep the call allocation-free (e.g. under CUDA-graph capture)."""
+    s, hq, d = q.shape
+    nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = decode_workspace_bytes(s, hq, d, mb, bs, num_splits)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().pa_paged_attention_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        s, hq, hkv, d, bs, nb, mb, float(scale or 0.0), _dtype(q), int(num_splits),
+        _ptr(out), _ptr(workspace), ws_len, _ptr(error_word), _stream(stream))
+    _check("pa_paged_attention_decode", st)
+    return out
+
+
+def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                           block_tables: torch.Tensor, max_query_len: int, causal: bool = True,
+                           scale: float | None = None, out: torch.Tensor | None = None,
+                           error_word: torch.Tensor | None = None,
+                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Flattened prefill / verify / decode batch; request r's queries are the newest q_len of
+    its seq_lens[r] positions, causal by position."""
+    n, hq, d = q.shape
+    nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    r = seq_lens.shape[0]
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    st = _lib.load().pa_paged_attention_varlen(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
+        r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
+        _dtype(q), _ptr(out), _ptr(error_word), _stream(stream))
+    _check("pa_paged_attention_varlen", st)
+    return out
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

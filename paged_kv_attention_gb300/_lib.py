@@ -1,0 +1,64 @@
+"""ctypes view of libpagedattn.so: the C ABI declared in include/paged_attn.h, nothing more."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpagedattn.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARGUMENT = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_WORKSPACE_TOO_SMALL = 3
+PA_ERR_CUDA = 4
+
+PA_DTYPE_F32 = 0
+PA_DTYPE_BF16 = 1
+
+PA_ERRBIT_PAGE_OUT_OF_POOL = 1
+PA_ERRBIT_LENGTH_OUT_OF_RANGE = 2
+PA_ERRBIT_SLOT_OUT_OF_POOL = 4
+PA_ERRBIT_QUERY_LAYOUT = 8
+PA_ERRBIT_WAIT_TIMEOUT = 16
+
+_i, _f, _p, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/paged_attn.h
+SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [_i]),
+    "pa_version": (_i, []),
+    "pa_supports": (_i, [_i, _i, _i, _i, _i, _i]),
+    "pa_plan_decode_splits": (_i, [_i, _i, _i, _i]),
+    "pa_decode_auto_splits": (_i, [_i, _i, _i, _i, _i, _i, _i]),
+    "pa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "pa_reshape_and_cache": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p]),
+    "pa_paged_attention_decode": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                                       _p, _p, _sz, _p, _p]),
+    "pa_paged_attention_varlen": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                       _i, _f, _i, _p, _p, _p]),
+}
+
+_lib = None
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library (built by ``paged_kv_attention_gb300.build``). Raises if absent:
+    there is no fallback implementation."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise LibraryMissing(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

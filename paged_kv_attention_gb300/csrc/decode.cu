@@ -1,0 +1,675 @@
+// Split-KV paged decode for sm_103a, and the log-sum-exp combine.
+//
+// Method ("TileInfer.jl - Attention kernels", Decode: GQA packing and split-KV;
+// "32. Production attention kernels", Long contexts: split the keys):
+//  * one CTA per (unit, KV head, split); the query heads that share the KV head form the
+//    rows of one query tile, so every page of keys and values is read from HBM once per
+//    group;
+//  * the CTA walks its share of the block table 16 tokens at a time: a producer warp reads
+//    the page id (a scalar load) and issues TMA loads of that page's rows for this KV head
+//    into a ring of shared-memory stages;
+//  * consumer warps take stages in turn and run the FlashAttention-2 online softmax with
+//    fp32 scores in the exp2 domain (scale pre-multiplied by log2 e);
+//  * a split writes its unnormalised partial (acc, m, l) to an fp32 workspace, or the
+//    normalised output directly when there is one split; empty splits write the neutral
+//    partial (0, -inf, 0) by the same arithmetic.
+//
+// bf16 path: the score and P.V products run on the tensor cores as mma.sync m16n8k16 with
+// keys on M (16 per stage) and the packed query rows on N (8 per tile, two tiles for
+// groups of 9-16). Decode does about 4 flops per byte of cache, so the tensor pipe is far
+// from the limit; the point of the MMA is to keep the issue slots free for the memory
+// pipeline. The probabilities are moved from the score accumulator layout to the P.V
+// operand layout with movmatrix (an in-register 8x8 transpose), without shared memory.
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// ------------------------------------------------------------------ unit resolution
+struct Unit {
+  int len;        // keys visible to every row of the unit: positions [0, len)
+  int table_row;  // block table row
+  int q_row;      // row of q / out
+};
+
+__device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bool report) {
+  Unit u;
+  int len;
+  if (!p.varlen) {
+    u.table_row = unit;
+    u.q_row = unit;
+    len = p.context_lens[unit];
+  } else {
+    // request r with query_start_loc[r] <= unit < query_start_loc[r+1]
+    int lo = 0, hi = p.num_reqs;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.query_start_loc[mid] <= unit) lo = mid; else hi = mid;
+    }
+    const int start = p.query_start_loc[lo];
+    const int stop = p.query_start_loc[lo + 1];
+    const int seq = p.seq_lens[lo];
+    const int q_len = stop - start;
+    u.table_row = lo;
+    u.q_row = unit;
+    if (unit < start || unit >= stop || q_len > seq) {
+      if (report) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
+      len = 0;
+    } else {
+      const int pos = seq - q_len + (unit - start);  // queries are the newest positions
+      len = p.causal ? pos + 1 : seq;
+    }
+  }
+  const int cap = p.max_blocks * p.block_size;
+  if (len < 0 || len > cap) {
+    if (report) flag_error(p.err, PA_ERRBIT_LENGTH_OUT_OF_RANGE);
+    len = len < 0 ? 0 : cap;
+  }
+  u.len = len;
+  return u;
+}
+
+// ------------------------------------------------------------------ epilogue
+// Merge the per-warp online-softmax states kept in shared memory and write either the
+// normalised rows (one split) or this split's unnormalised partial.
+//   mo: [nw][rows][D] accumulators, ml: [nw][rows][2] (m in log2 units, l)
+template <typename OutT>
+__device__ __forceinline__ void merge_and_store(const DecodeParams& p, const float* mo, const float* ml, int nw,
+                                                int rows, int D, int unit, int q_row, int kvh, int split) {
+  const int G = p.group;
+  const int h0 = kvh * G;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int n = idx / D;
+    const int d = idx - n * D;
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, ml[(w * rows + n) * 2]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, O = 0.f;
+    for (int w = 0; w < nw; ++w) {
+      const float wt = exp2f(ml[(w * rows + n) * 2] - Mu);
+      L += wt * ml[(w * rows + n) * 2 + 1];
+      O += wt * mo[(w * rows + n) * D + d];
+    }
+    if (p.num_splits == 1) {
+      const float v = (L > 0.f) ? O / L : 0.f;
+      OutT* out = reinterpret_cast<OutT*>(p.out);
+      out[((size_t)q_row * p.num_q_heads + h0 + n) * D + d] = static_cast<OutT>(v);
+    } else {
+      const size_t slot = ((size_t)unit * p.num_splits + split) * p.num_q_heads + h0 + n;
+      p.ws_acc[slot * D + d] = O;
+      if (d == 0) {
+        p.ws_ml[slot * 2] = M;
+        p.ws_ml[slot * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ bf16 tensor-core decode
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <int D>
+struct Bf16Cfg {
+  static constexpr int kConsumers = 4;
+  static constexpr int kThreads = (kConsumers + 1) * 32;
+  static constexpr int kDChunks = D / 64;                 // 128-byte swizzle columns
+  static constexpr int kTileBytes = kChunk * D * 2;       // K or V rows of one stage
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = (D == 64) ? 16 : (D == 128 ? 8 : 4);  // 64 KiB ring
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kMT = D / 16;
+  // barriers + merge (m, l) after the ring; the merge accumulators alias the ring
+  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kConsumers * 16 * 2 * 4;
+  static_assert(kStages % kConsumers == 0, "stages are dealt to consumers round robin");
+  static_assert(kConsumers * 16 * D * 4 <= kRingBytes, "merge area must fit in the ring");
+};
+
+template <int D, int NT>
+__global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
+    decode_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap) {
+  using C = Bf16Cfg<D>;
+  constexpr int ROWS = 8 * NT;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared window
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
+  uint64_t* empty = full + C::kStages;
+  float* merge_ml = reinterpret_cast<float*>(empty + C::kStages);  // [consumers][ROWS][2]
+  float* merge_o = reinterpret_cast<float*>(smem);                 // aliases the ring after the loop
+  __shared__ int s_timeout;
+  __shared__ int s_issued;
+
+  const int unit = blockIdx.x / p.num_splits;
+  const int split = blockIdx.x - unit * p.num_splits;
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
+  const int n_chunks = (u.len + kChunk - 1) / kChunk;
+  const int c_begin = split * p.chunks_per_split;
+  const int c_end = min(n_chunks, c_begin + p.chunks_per_split);
+  const int n_mine = max(0, c_end - c_begin);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    fence_barrier_init();
+    s_timeout = 0;
+    s_issued = 0;
+  }
+  __syncthreads();
+
+  if (warp == C::kConsumers) {
+    // ---------------- producer: page-table walk + TMA
+    if (lane == 0 && n_mine > 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+      const int32_t* table = p.block_tables + (size_t)u.table_row * p.max_blocks;
+      int issued = 0;
+      for (int i = 0; i < n_mine; ++i) {
+        const int stage = i % C::kStages;
+        if (i >= C::kStages && !mbar_wait(&empty[stage], ((i / C::kStages) - 1) & 1)) {
+          flag_error(p.err, PA_ERRBIT_WAIT_TIMEOUT);
+          atomicExch(&s_timeout, 1);
+          break;
+        }
+        const int tok = (c_begin + i) * kChunk;
+        const int page_idx = tok / p.block_size;
+        const int in_page = tok - page_idx * p.block_size;
+        const int page = table[page_idx];
+        if (page < 0 || page >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // TMA reads zeros
+        uint8_t* st = smem + stage * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+#pragma unroll
+        for (int a = 0; a < C::kDChunks; ++a)
+          tma_load_4d(st + a * (kChunk * 128), &kmap, &full[stage], a * 64, kvh, in_page, page);
+#pragma unroll
+        for (int a = 0; a < C::kDChunks; ++a)
+          tma_load_4d(st + C::kTileBytes + a * (kChunk * 128), &vmap, &full[stage], a * 64, kvh, in_page, page);
+        issued = i + 1;
+      }
+      s_issued = issued;
+    }
+  } else {
+    // ---------------- consumers
+    const int G = p.group;
+    const int g4 = lane >> 2;  // groupID
+    const int t4 = lane & 3;   // thread in group
+    // Q^T as the B operand: rows n (query heads of the group), k = head dim
+    uint32_t qf[NT][C::kMT][2];
+    {
+      const __nv_bfloat16* qb =
+          reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)u.q_row * p.num_q_heads + (size_t)kvh * G) * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + g4;
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + (size_t)n * D);
+#pragma unroll
+        for (int kk = 0; kk < C::kMT; ++kk) {
+          qf[nt][kk][0] = (n < G) ? __ldg(qr + (kk * 16 + 2 * t4) / 2) : 0u;
+          qf[nt][kk][1] = (n < G) ? __ldg(qr + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
+        }
+      }
+    }
+    float o[NT][C::kMT][4];
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < C::kMT; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    }
+    const float sl2 = p.scale_log2;
+    // ldmatrix lane addressing: matrix mi = lane/8 supplies row ri = lane%8
+    const int mi = lane >> 3, ri = lane & 7;
+    const int k_key = ri + 8 * (mi & 1), k_unit = mi >> 1;  // K: (keys 0-7|8-15) x (unit u0|u0+1)
+    const int v_key = ri + 8 * (mi >> 1), v_unit = mi & 1;  // V^T: (d 0-7|8-15) x (keys 0-7|8-15)
+
+    for (int i = warp; i < n_mine; i += C::kConsumers) {
+      const int stage = i % C::kStages;
+      if (!mbar_wait(&full[stage], (i / C::kStages) & 1)) {
+        flag_error(p.err, PA_ERRBIT_WAIT_TIMEOUT);
+        atomicExch(&s_timeout, 1);
+        break;
+      }
+      uint8_t* kt = smem + stage * C::kStageBytes;
+      uint8_t* vt = kt + C::kTileBytes;
+      const int key0 = (c_begin + i) * kChunk;
+      const int nvalid = min(kChunk, u.len - key0);
+      if (nvalid < kChunk) {
+        // rows past the sequence end may hold anything (NaN included): zero them so that
+        // 0-probability keys contribute exactly 0 to P.V (a select, not a multiply)
+        for (int idx = lane; idx < (kChunk - nvalid) * C::kDChunks * 8; idx += 32) {
+          const int row = nvalid + idx / (C::kDChunks * 8);
+          const int rest = idx % (C::kDChunks * 8);
+          reinterpret_cast<uint4*>(vt + (rest / 8) * (kChunk * 128) + row * 128)[rest % 8] = make_uint4(0, 0, 0, 0);
+        }
+        // these generic-proxy writes precede the next TMA write of this stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      // S^T[16 keys x 8 rows] = K . Q^T
+      float s[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < C::kMT; ++kk) {
+        uint32_t a[4];
+        const int dch = kk >> 2;
+        const int unit_idx = 2 * (kk & 3) + k_unit;
+        ldsm_x4(a, smem_addr(kt + dch * (kChunk * 128) + swz128(k_key, unit_idx)));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+      }
+      // online softmax (rows 2*t4 and 2*t4+1; keys g4 and g4+8)
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float x0 = s[nt][0] * sl2, x1 = s[nt][1] * sl2, x2 = s[nt][2] * sl2, x3 = s[nt][3] * sl2;
+        if (g4 >= nvalid) x0 = x1 = -INFINITY;
+        if (g4 + 8 >= nvalid) x2 = x3 = -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+        const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const float al0 = exp2f(m_run[nt][0] - mu0), al1 = exp2f(m_run[nt][1] - mu1);
+        const float p0 = exp2f(x0 - mu0), p2 = exp2f(x2 - mu0);
+        const float p1 = exp2f(x1 - mu1), p3 = exp2f(x3 - mu1);
+        l_run[nt][0] = l_run[nt][0] * al0 + p0 + p2;
+        l_run[nt][1] = l_run[nt][1] * al1 + p1 + p3;
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt) {
+          o[nt][mt][0] *= al0;
+          o[nt][mt][1] *= al1;
+          o[nt][mt][2] *= al0;
+          o[nt][mt][3] *= al1;
+        }
+        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
+        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
+      }
+      // O^T[d x rows] += V^T . P^T
+#pragma unroll
+      for (int mt = 0; mt < C::kMT; ++mt) {
+        uint32_t a[4];
+        const int dch = mt >> 2;
+        const int unit_idx = 2 * (mt & 3) + v_unit;
+        ldsm_x4_trans(a, smem_addr(vt + dch * (kChunk * 128) + swz128(v_key, unit_idx)));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    // full row sums: the 8 threads of a row each hold a share of l
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) l_run[nt][j] += __shfl_xor_sync(0xffffffffu, l_run[nt][j], off);
+    // hand the state to the merge (the ring is free once every consumer is past its loop)
+    asm volatile("bar.sync 1, %0;" ::"n"(C::kConsumers * 32));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int n = nt * 8 + 2 * t4 + j;
+        if (g4 == 0) {
+          merge_ml[(warp * ROWS + n) * 2] = m_run[nt][j];
+          merge_ml[(warp * ROWS + n) * 2 + 1] = l_run[nt][j];
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt) {
+          merge_o[(warp * ROWS + n) * D + mt * 16 + g4] = o[nt][mt][j];
+          merge_o[(warp * ROWS + n) * D + mt * 16 + g4 + 8] = o[nt][mt][2 + j];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (s_timeout && threadIdx.x == C::kConsumers * 32) {
+    // wind down: let copies still in flight land before the CTA's shared memory is released
+    const int issued = s_issued;
+    for (int i = max(0, issued - C::kStages); i < issued; ++i)
+      (void)mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1);
+  }
+  __syncthreads();
+  merge_and_store<__nv_bfloat16>(p, merge_o, merge_ml, C::kConsumers, ROWS, D, unit, u.q_row, kvh, split);
+}
+
+// ------------------------------------------------------------------ fp32 CUDA-core decode
+// Lanes take keys for the scores (each lane one key, the group's query rows broadcast from
+// shared memory) and head-dim columns for P.V. fp32 throughout, no TF32.
+template <int D, int GP>
+struct F32Cfg {
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kSmemBytes =
+      (GP * D + kWarps * GP * 32 + kWarps * GP * D + kWarps * GP * 2) * 4 + kWarps * 32 * 8;
+};
+
+template <int D, int GP>
+__global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__ DecodeParams p) {
+  using C = F32Cfg<D, GP>;
+  constexpr int DL = D / 32;  // columns per lane
+  extern __shared__ float fsm[];
+  float* q_s = fsm;                               // [GP][D]
+  float* p_s = q_s + GP * D;                      // [warps][GP][32]
+  float* merge_o = p_s + C::kWarps * GP * 32;     // [warps][GP][D]
+  float* merge_ml = merge_o + C::kWarps * GP * D; // [warps][GP][2]
+  long long* vrow_s = reinterpret_cast<long long*>(merge_ml + C::kWarps * GP * 2);  // [warps][32]
+
+  const int unit = blockIdx.x / p.num_splits;
+  const int split = blockIdx.x - unit * p.num_splits;
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
+  const int k_begin = split * p.chunks_per_split * kChunk;
+  const int k_end = min(u.len, k_begin + p.chunks_per_split * kChunk);
+
+  const float* qg = reinterpret_cast<const float*>(p.q) + ((size_t)u.q_row * p.num_q_heads + (size_t)kvh * G) * D;
+  for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) q_s[idx] = (idx / D < G) ? qg[idx] : 0.f;
+  __syncthreads();
+
+  const float* kc = reinterpret_cast<const float*>(p.k_cache);
+  const float* vc = reinterpret_cast<const float*>(p.v_cache);
+  const int32_t* table = p.block_tables + (size_t)u.table_row * p.max_blocks;
+  const size_t row_elems = (size_t)p.num_kv_heads * D;
+  float m_run[GP], l_run[GP], acc[GP][DL];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    m_run[g] = -INFINITY;
+    l_run[g] = 0.f;
+#pragma unroll
+    for (int j = 0; j < DL; ++j) acc[g][j] = 0.f;
+  }
+  float* my_p = p_s + warp * GP * 32;
+  long long* my_vrow = vrow_s + warp * 32;
+  for (int kb = k_begin + warp * 32; kb < k_end; kb += C::kWarps * 32) {
+    const int key = kb + lane;
+    const bool valid = key < k_end;
+    long long row = 0;
+    if (valid) {
+      int page = table[key / p.block_size];
+      if (page < 0 || page >= p.num_blocks) {
+        flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);
+        page = -1;
+      }
+      row = (page < 0) ? -1 : ((long long)page * p.block_size + key % p.block_size);
+    }
+    float s[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) s[g] = 0.f;
+    if (valid && row >= 0) {
+      const float4* kr = reinterpret_cast<const float4*>(kc + (size_t)row * row_elems + (size_t)kvh * D);
+#pragma unroll 4
+      for (int d4 = 0; d4 < D / 4; ++d4) {
+        const float4 k4 = __ldg(kr + d4);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float4 q4 = reinterpret_cast<const float4*>(q_s + g * D)[d4];
+          s[g] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, s[g]))));
+        }
+      }
+    }
+    my_vrow[lane] = valid ? row : -2;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      const float x = valid ? s[g] * p.scale_log2 : -INFINITY;
+      float mx = x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m_run[g], mx);
+      const float mu = (mn == -INFINITY) ? 0.f : mn;
+      const float al = exp2f(m_run[g] - mu);
+      const float pr = valid ? exp2f(x - mu) : 0.f;
+      l_run[g] = l_run[g] * al + pr;
+      m_run[g] = mn;
+#pragma unroll
+      for (int j = 0; j < DL; ++j) acc[g][j] *= al;
+      my_p[g * 32 + lane] = pr;
+    }
+    __syncwarp();
+    const int nk = min(32, k_end - kb);
+    for (int j = 0; j < nk; ++j) {
+      const long long vr = my_vrow[j];
+      if (vr < 0) continue;  // a page outside the pool contributes nothing
+      const float* vrp = vc + (size_t)vr * row_elems + (size_t)kvh * D;
+      float vv[DL];
+#pragma unroll
+      for (int c = 0; c < DL; ++c) vv[c] = __ldg(vrp + lane + 32 * c);
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float pj = my_p[g * 32 + j];
+#pragma unroll
+        for (int c = 0; c < DL; ++c) acc[g][c] = fmaf(pj, vv[c], acc[g][c]);
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], off);
+    if (lane == 0) {
+      merge_ml[(warp * GP + g) * 2] = m_run[g];
+      merge_ml[(warp * GP + g) * 2 + 1] = l_run[g];
+    }
+#pragma unroll
+    for (int c = 0; c < DL; ++c) merge_o[(warp * GP + g) * D + lane + 32 * c] = acc[g][c];
+  }
+  __syncthreads();
+  merge_and_store<float>(p, merge_o, merge_ml, C::kWarps, GP, D, unit, u.q_row, kvh, split);
+}
+
+// ------------------------------------------------------------------ combine
+// One warp per (unit, query head): M = max_s m_s, w_s = 2^(m_s - M),
+// out = sum_s w_s acc_s / sum_s w_s l_s; an all-empty row (M = -inf) gives zeros.
+// ("32. Production attention kernels", Long contexts: split the keys, the merge;
+//  "poot - Attention and KV Cache", Split-KV decode, Combine.)
+template <typename OutT>
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeParams p) {
+  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= p.num_units * p.num_q_heads) return;
+  const int unit = gw / p.num_q_heads;
+  const int h = gw - unit * p.num_q_heads;
+  const int S = p.num_splits;
+  const int D = p.head_dim;
+  const size_t base = (size_t)unit * S * p.num_q_heads + h;  // slot of split s: base + s * Hq
+  const float m_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2] : -INFINITY;
+  const float l_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2 + 1] : 0.f;
+  float M = m_s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  const float w = (lane < S) ? exp2f(m_s - Mu) : 0.f;
+  float L = w * l_s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)unit * p.num_q_heads + h) * D;
+  for (int d = lane * 4; d < D; d += 128) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)s * p.num_q_heads) * D + d);
+      a.x = fmaf(ws, v.x, a.x);
+      a.y = fmaf(ws, v.y, a.y);
+      a.z = fmaf(ws, v.z, a.z);
+      a.w = fmaf(ws, v.w, a.w);
+    }
+    out[d] = static_cast<OutT>(a.x * inv);
+    out[d + 1] = static_cast<OutT>(a.y * inv);
+    out[d + 2] = static_cast<OutT>(a.z * inv);
+    out[d + 3] = static_cast<OutT>(a.w * inv);
+  }
+}
+
+template <int D, int NT>
+cudaError_t launch_bf16_impl(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream) {
+  using C = Bf16Cfg<D>;
+  auto kern = decode_bf16_kernel<D, NT>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  dim3 grid((unsigned)(p.num_units * p.num_splits), (unsigned)p.num_kv_heads, 1);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, kmap, vmap);
+  return cudaGetLastError();
+}
+
+template <int D, int NT>
+int occupancy_bf16() {
+  using C = Bf16Cfg<D>;
+  auto kern = decode_bf16_kernel<D, NT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmemBytes) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+template <int D, int GP>
+cudaError_t launch_f32_impl(const DecodeParams& p, cudaStream_t stream) {
+  using C = F32Cfg<D, GP>;
+  auto kern = decode_f32_kernel<D, GP>;
+  if (C::kSmemBytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((unsigned)(p.num_units * p.num_splits), (unsigned)p.num_kv_heads, 1);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int GP>
+int occupancy_f32() {
+  using C = F32Cfg<D, GP>;
+  auto kern = decode_f32_kernel<D, GP>;
+  if (C::kSmemBytes > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmemBytes) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+int pad_group(int g) {
+  int gp = 1;
+  while (gp < g) gp <<= 1;
+  return gp;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t stream) {
+  const bool two = p.group > 8;
+  switch (p.head_dim) {
+    case 64: return two ? launch_bf16_impl<64, 2>(p, kmap, vmap, stream) : launch_bf16_impl<64, 1>(p, kmap, vmap, stream);
+    case 128: return two ? launch_bf16_impl<128, 2>(p, kmap, vmap, stream) : launch_bf16_impl<128, 1>(p, kmap, vmap, stream);
+    case 256: return two ? launch_bf16_impl<256, 2>(p, kmap, vmap, stream) : launch_bf16_impl<256, 1>(p, kmap, vmap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int decode_bf16_ctas_per_sm(int head_dim, int group) {
+  const bool two = group > 8;
+  switch (head_dim) {
+    case 64: return two ? occupancy_bf16<64, 2>() : occupancy_bf16<64, 1>();
+    case 128: return two ? occupancy_bf16<128, 2>() : occupancy_bf16<128, 1>();
+    case 256: return two ? occupancy_bf16<256, 2>() : occupancy_bf16<256, 1>();
+    default: return 1;
+  }
+}
+
+#define PA_F32_CASES(D)                                         \
+  switch (pad_group(p.group)) {                                 \
+    case 1: return launch_f32_impl<D, 1>(p, stream);            \
+    case 2: return launch_f32_impl<D, 2>(p, stream);            \
+    case 4: return launch_f32_impl<D, 4>(p, stream);            \
+    case 8: return launch_f32_impl<D, 8>(p, stream);            \
+    case 16: if (D <= 128) return launch_f32_impl<(D <= 128 ? D : 128), 16>(p, stream); \
+             return cudaErrorInvalidValue;                      \
+    default: return cudaErrorInvalidValue;                      \
+  }
+
+cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream) {
+  switch (p.head_dim) {
+    case 64: PA_F32_CASES(64)
+    case 128: PA_F32_CASES(128)
+    case 256: PA_F32_CASES(256)
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+#define PA_F32_OCC(D)                                           \
+  switch (pad_group(group)) {                                   \
+    case 1: return occupancy_f32<D, 1>();                       \
+    case 2: return occupancy_f32<D, 2>();                       \
+    case 4: return occupancy_f32<D, 4>();                       \
+    case 8: return occupancy_f32<D, 8>();                       \
+    case 16: return occupancy_f32<(D <= 128 ? D : 128), 16>();  \
+    default: return 1;                                          \
+  }
+
+int decode_f32_ctas_per_sm(int head_dim, int group) {
+  switch (head_dim) {
+    case 64: PA_F32_OCC(64)
+    case 128: PA_F32_OCC(128)
+    case 256: PA_F32_OCC(256)
+    default: return 1;
+  }
+}
+
+cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
+  const long long warps = (long long)p.num_units * p.num_q_heads;
+  const unsigned blocks = (unsigned)((warps + 3) / 4);
+  if (dtype == PA_DTYPE_BF16)
+    combine_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(p);
+  else
+    combine_kernel<float><<<blocks, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

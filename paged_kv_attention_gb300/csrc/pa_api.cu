@@ -1,0 +1,383 @@
+// C-ABI entry points: argument validation, split planning, TMA descriptor encoding and
+// launches on the caller's stream. Nothing here allocates device memory or synchronises.
+#include <math.h>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+long long cdivll(long long a, long long b) { return (a + b - 1) / b; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [num_blocks, block_size, Hkv, D] bf16 pool viewed as a 4-D tensor (D, Hkv, bs, blocks);
+// one box is `box_tokens` rows of one KV head, 64 columns (128 bytes, swizzled).
+bool encode_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs, int num_blocks, int box_tokens) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)bs, (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)bs * Hkv * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tokens, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// q [N, Hq, D] bf16 viewed as (D, Hq, N); one box = `tokens` tokens x `group` heads x 64 cols.
+bool encode_query_map(CUtensorMap* map, const void* base, int D, int Hq, int N, int group, int tokens) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)tokens};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int occ_bf16[3][2] = {};  // [D 64/128/256][group <= 8 | > 8]
+  int occ_f32[3][5] = {};   // [D][padded group 1..16]
+};
+
+bool device_info(DeviceInfo** out) {
+  static DeviceInfo infos[64];
+  static bool ready[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ready[dev]) {
+    if (cudaDeviceGetAttribute(&infos[dev].sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    ready[dev] = true;
+  }
+  *out = &infos[dev];
+  return true;
+}
+
+int dim_index(int d) { return d == 64 ? 0 : (d == 128 ? 1 : 2); }
+int log2i(int g) {
+  int l = 0;
+  while ((1 << l) < g) ++l;
+  return l;
+}
+
+bool group_ok_bf16(int G) { return G >= 1 && G <= 16; }
+bool group_ok_f32(int G, int D) { return G >= 1 && G <= 16 && G * D <= 2048; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARGUMENT: return "PA_ERR_INVALID_ARGUMENT";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "PA_ERR_WORKSPACE_TOO_SMALL";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int pa_version(void) { return kVersion; }
+
+extern "C" int pa_supports(int is_varlen, int head_dim, int num_q_heads, int num_kv_heads, int block_size,
+                           pa_dtype dtype) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0) return 0;
+  if (!valid_head_dim(head_dim)) return 0;
+  const int G = num_q_heads / num_kv_heads;
+  if (dtype == PA_DTYPE_BF16) return group_ok_bf16(G) && block_size % kChunk == 0 ? 1 : 0;
+  if (dtype == PA_DTYPE_F32) return group_ok_f32(G, head_dim) ? 1 : 0;
+  (void)is_varlen;
+  return 0;
+}
+
+extern "C" int pa_plan_decode_splits(int num_units, int max_chunks, int num_sms, int ctas_per_sm) {
+  if (num_units <= 0 || max_chunks <= 0 || num_sms <= 0 || ctas_per_sm <= 0) return 1;
+  // No split shorter than 4 chunks (64 tokens), none at all past 32, and never more splits
+  // than chunks (empty trailing splits would only cost the combine).
+  constexpr int kMinChunksPerSplit = 4;
+  const int cap = (int)std::max<long long>(1, std::min<long long>(kMaxSplits, max_chunks / kMinChunksPerSplit));
+  const long long slots = (long long)num_sms * ctas_per_sm;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= cap; ++s) {
+    // splits whose boundaries fall on the same chunks are one choice: keep the smallest
+    const long long per = cdivll(max_chunks, s);
+    if (cdivll(max_chunks, per) != s) continue;
+    const long long ctas = (long long)num_units * s;
+    const long long waves = cdivll(ctas, slots);
+    const double eff = (double)ctas / (double)(waves * slots);
+    if (eff > best_eff + 0.02) {  // a larger count must fill waves clearly better to win
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
+                                            int block_size, int num_splits) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0) return 0;
+  const long long max_chunks = cdivll((long long)max_blocks_per_seq * block_size, kChunk);
+  long long splits;
+  if (num_splits <= 0) {
+    splits = std::min<long long>(kMaxSplits, std::max<long long>(1, max_chunks / 4));
+  } else {
+    splits = std::min<long long>(num_splits, max_chunks);
+  }
+  if (splits <= 1) return 0;
+  const long long per_slot = (long long)head_dim + 2;
+  return (size_t)((long long)num_seqs * splits * num_q_heads * per_slot * 4);
+}
+
+extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                          const int32_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                          int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                                          int32_t* error_word, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARGUMENT;
+  const int elem = dtype == PA_DTYPE_BF16 ? 2 : 4;
+  const long long row_bytes = (long long)num_kv_heads * head_dim * elem;
+  if (row_bytes % 16 != 0 || row_bytes > (1ll << 30)) return PA_ERR_UNSUPPORTED;
+  const long long num_slots = (long long)num_blocks * block_size;
+  cudaError_t e = launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, (int)row_bytes,
+                                           num_slots, error_word, as_stream(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+namespace {
+
+pa_status validate_common(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          const void* out, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, int max_blocks_per_seq, float scale, pa_dtype dtype) {
+  if (!q || !k_cache || !v_cache || !block_tables || !out) return PA_ERR_INVALID_ARGUMENT;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARGUMENT;
+  if (head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (!(scale >= 0.f) || isinf(scale)) return PA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID_ARGUMENT;
+  if ((long long)max_blocks_per_seq * block_size > (1ll << 30)) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
+  if (!valid_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  if (dtype == PA_DTYPE_BF16 && (!group_ok_bf16(G) || block_size % kChunk != 0)) return PA_ERR_UNSUPPORTED;
+  if (dtype == PA_DTYPE_F32 && !group_ok_f32(G, head_dim)) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long max_chunks, pa_dtype dtype) {
+  int occ;
+  if (dtype == PA_DTYPE_BF16) {
+    int& slot = info->occ_bf16[dim_index(D)][G > 8 ? 1 : 0];
+    if (slot == 0) slot = decode_bf16_ctas_per_sm(D, G);
+    occ = slot;
+  } else {
+    int& slot = info->occ_f32[dim_index(D)][log2i(G)];
+    if (slot == 0) slot = decode_f32_ctas_per_sm(D, G);
+    occ = slot;
+  }
+  int s = pa_plan_decode_splits(units * Hkv, (int)std::min<long long>(max_chunks, 1 << 30), info->sms, occ);
+  s = (int)std::min<long long>(s, max_chunks);
+  const long long per = cdivll(max_chunks, s);
+  return (int)cdivll(max_chunks, per);
+}
+
+// Launch the decode-style kernels over `p.num_units` units (already filled in except the
+// split fields), then the combine when splitting.
+pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache, const void* v_cache,
+                           int requested_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  DeviceInfo* info = nullptr;
+  if (!device_info(&info)) return PA_ERR_CUDA;
+  const int D = p.head_dim;
+  const long long max_chunks = cdivll((long long)p.max_blocks * p.block_size, kChunk);
+  int splits = requested_splits;
+  if (splits <= 0) splits = auto_splits(info, p.num_units, p.num_kv_heads, D, p.group, max_chunks, dtype);
+  splits = (int)std::min<long long>(splits, max_chunks);
+  const int per = (int)cdivll(max_chunks, splits);
+  splits = (int)cdivll(max_chunks, per);
+  p.num_splits = splits;
+  p.chunks_per_split = per;
+  if (splits > 1) {
+    const size_t need = (size_t)p.num_units * splits * p.num_q_heads * ((size_t)D + 2) * 4;
+    if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return PA_ERR_INVALID_ARGUMENT;
+    p.ws_acc = static_cast<float*>(workspace);
+    p.ws_ml = p.ws_acc + (size_t)p.num_units * splits * p.num_q_heads * D;
+  }
+  cudaError_t e;
+  if (dtype == PA_DTYPE_BF16) {
+    CUtensorMap kmap, vmap;
+    if (!encode_cache_map(&kmap, k_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk) ||
+        !encode_cache_map(&vmap, v_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk))
+      return PA_ERR_CUDA;
+    e = launch_decode_bf16(p, kmap, vmap, stream);
+  } else {
+    e = launch_decode_f32(p, stream);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (splits > 1) {
+    e = launch_combine(p, dtype, stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_auto_splits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                     int max_blocks_per_seq, pa_dtype dtype) {
+  if (num_seqs <= 0) return 0;
+  static const int dummy[4] __attribute__((aligned(16))) = {};
+  if (validate_common(dummy, dummy, dummy, dummy, dummy, num_q_heads, num_kv_heads, head_dim, block_size, 1,
+                      max_blocks_per_seq, 0.f, dtype) != PA_OK)
+    return 0;
+  DeviceInfo* info = nullptr;
+  if (!device_info(&info)) return 0;
+  const long long max_chunks = cdivll((long long)max_blocks_per_seq * block_size, kChunk);
+  return auto_splits(info, num_seqs, num_kv_heads, head_dim, num_q_heads / num_kv_heads, max_chunks, dtype);
+}
+
+extern "C" pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                               const int32_t* block_tables, const int32_t* context_lens,
+                                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                               int block_size, int num_blocks, int max_blocks_per_seq, float scale,
+                                               pa_dtype dtype, int num_splits, void* out, void* workspace,
+                                               size_t workspace_bytes, int32_t* error_word, void* stream) {
+  if (num_seqs < 0 || num_splits < 0 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0) return PA_OK;
+  if (!context_lens) return PA_ERR_INVALID_ARGUMENT;
+  pa_status st = validate_common(q, k_cache, v_cache, block_tables, out, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, num_blocks, max_blocks_per_seq, scale, dtype);
+  if (st != PA_OK) return st;
+  if ((long long)num_seqs * num_kv_heads * kMaxSplits > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = error_word;
+  p.varlen = 0;
+  p.causal = 0;
+  p.num_units = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+  p.scale_log2 = sc * kLog2e;
+  return run_decode_units(p, dtype, k_cache, v_cache, num_splits, workspace, workspace_bytes, as_stream(stream));
+}
+
+extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                                               const int32_t* block_tables, int num_reqs, int num_tokens,
+                                               int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                               int block_size, int num_blocks, int max_blocks_per_seq, int causal,
+                                               float scale, pa_dtype dtype, void* out, int32_t* error_word,
+                                               void* stream) {
+  if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
+  if (num_reqs == 0 || num_tokens == 0) return PA_OK;
+  if (!query_start_loc || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
+  pa_status st = validate_common(q, k_cache, v_cache, block_tables, out, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, num_blocks, max_blocks_per_seq, scale, dtype);
+  if (st != PA_OK) return st;
+  if ((long long)num_tokens * num_kv_heads > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+  cudaStream_t s = as_stream(stream);
+
+  if (dtype == PA_DTYPE_BF16 && varlen_tc_supported(head_dim, G, block_size) && max_query_len > 0) {
+    VarlenParams vp{};
+    vp.query_start_loc = query_start_loc;
+    vp.seq_lens = seq_lens;
+    vp.block_tables = block_tables;
+    vp.out = out;
+    vp.err = error_word;
+    vp.num_reqs = num_reqs;
+    vp.num_tokens = num_tokens;
+    vp.num_q_heads = num_q_heads;
+    vp.num_kv_heads = num_kv_heads;
+    vp.group = G;
+    vp.block_size = block_size;
+    vp.num_blocks = num_blocks;
+    vp.max_blocks = max_blocks_per_seq;
+    vp.max_query_len = max_query_len;
+    const int tokens_per_tile = 128 / G;
+    vp.q_tiles = (int)cdivll(max_query_len, tokens_per_tile);
+    vp.causal = causal ? 1 : 0;
+    vp.scale_log2 = sc * kLog2e;
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile) ||
+        !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks,
+                          block_size < 128 ? block_size : 128) ||
+        !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks,
+                          block_size < 128 ? block_size : 128))
+      return PA_ERR_CUDA;
+    return launch_varlen_tc(vp, qmap, kmap, vmap, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+
+  // Generic path: every query token is a decode over the keys it sees (one split).
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.query_start_loc = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.err = error_word;
+  p.varlen = 1;
+  p.causal = causal ? 1 : 0;
+  p.num_reqs = num_reqs;
+  p.num_units = num_tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = G;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.scale_log2 = sc * kLog2e;
+  return run_decode_units(p, dtype, k_cache, v_cache, 1, nullptr, 0, s);
+}

@@ -1,0 +1,87 @@
+// Internal host-side interface between the C-ABI entry points and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/paged_attn.h"
+
+namespace pa {
+
+constexpr int kMaxSplits = 32;
+constexpr int kChunk = 16;  // tokens per decode pipeline stage
+
+// Everything a decode-style kernel needs. A "unit" is one query row set that shares a
+// context: a sequence (decode) or a single query token of a varlen request (varlen
+// generic path). Work is grid (unit * num_splits + split, kv head).
+struct DecodeParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;     // decode: [units]
+  const int32_t* query_start_loc;  // varlen: [num_reqs + 1]
+  const int32_t* seq_lens;         // varlen: [num_reqs]
+  void* out;
+  float* ws_acc;  // [units, splits, Hq, D] when num_splits > 1
+  float* ws_ml;   // [units, splits, Hq, 2]
+  int32_t* err;
+  int varlen;
+  int causal;
+  int num_reqs;
+  int num_units;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  int max_blocks;
+  int num_splits;
+  int chunks_per_split;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                     const int32_t* slot_mapping, int num_tokens, int row_bytes,
+                                     long long num_slots, int32_t* err, cudaStream_t stream);
+
+// bf16 tensor-core decode (TMA page loads, mma.sync, 16-token chunks).
+cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t stream);
+int decode_bf16_ctas_per_sm(int head_dim, int group);
+
+// fp32 CUDA-core decode.
+cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream);
+int decode_f32_ctas_per_sm(int head_dim, int group);
+
+// log-sum-exp merge of split partials into out.
+cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
+
+// tcgen05 varlen kernel (bf16, head_dim 128).
+struct VarlenParams {
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  void* out;
+  int32_t* err;
+  int num_reqs;
+  int num_tokens;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int block_size;
+  int num_blocks;
+  int max_blocks;
+  int max_query_len;
+  int q_tiles;  // cdiv(max_query_len, tokens per tile)
+  int causal;
+  float scale_log2;
+};
+bool varlen_tc_supported(int head_dim, int group, int block_size);
+cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, cudaStream_t stream);
+
+}  // namespace pa

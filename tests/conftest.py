@@ -24,3 +24,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionstart(session):
+    """Rebuild the in-tree CUDA library when a source is newer than it (nvcc cross-compiles
+    without a GPU), so every test runs the current kernels."""
+    from paged_kv_attention_gb300 import build
+    if build.is_stale():
+        build.build()

@@ -1,0 +1,120 @@
+"""GPU parity of pa_paged_attention_varlen (prefill chunks, decodes and verify blocks in one
+flattened batch, causal by position) against the float64 oracle."""
+
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_gb300 as pa
+import workloads
+from paged_helpers import check_close, gpu_pools, named_case, oracle_pools
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_varlen(case, kc, vc, causal=None, **kw):
+    return pa.paged_attention_varlen(case.q.to(DEV), kc, vc, case.query_start_loc.to(DEV),
+                                     case.seq_lens.to(DEV), case.block_tables.to(DEV), case.max_query_len,
+                                     case.causal if causal is None else causal, case.scale, **kw)
+
+
+def oracle_varlen(case, ko, vo, causal=None, tokens=None):
+    return oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, case.seq_lens,
+                                         case.block_tables, case.causal if causal is None else causal,
+                                         case.scale, tokens=tokens)
+
+
+def sample_tokens(case, stride=23, edge=40):
+    """Every decode / verify token, both ends of every long query block, and a stride sample."""
+    qsl = case.query_start_loc.tolist()
+    picked = set()
+    for r in range(case.num_reqs):
+        a, b = qsl[r], qsl[r + 1]
+        if b - a <= 2 * edge:
+            picked.update(range(a, b))
+        else:
+            picked.update(range(a, a + edge))
+            picked.update(range(b - edge, b))
+            picked.update(range(a, b, stride))
+    return torch.tensor(sorted(picked))
+
+
+def test_mixed_batch():
+    case, (ko, vo) = named_case("varlen_mixed_bf16")
+    kc, vc = gpu_pools(case)
+    out = run_varlen(case, kc, vc)
+    rows = sample_tokens(case)
+    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), case.dtype, rows=rows, label="mixed")
+
+
+def test_long_causal_prefill_sampled():
+    case, (ko, vo) = named_case("prefill_4x8192_bf16")
+    kc, vc = gpu_pools(case)
+    out = run_varlen(case, kc, vc)
+    rows = sample_tokens(case, stride=331, edge=150)
+    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), case.dtype, rows=rows, label="prefill 4x8192")
+    # a property every row must have, at full size: finite, and bounded by the values' range
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("head_dim,hq,hkv,bs", [(128, 32, 8, 16), (128, 8, 8, 16), (64, 16, 2, 32),
+                                                 (256, 8, 4, 64), (128, 16, 1, 64), (128, 4, 2, 128)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_small_mixed_batches(dtype, head_dim, hq, hkv, bs, causal):
+    if dtype == torch.float32 and (hq // hkv) * head_dim > 2048:
+        pytest.skip("f32 path covers group * head_dim <= 2048")
+    q_lens = [37, 1, 5, 0, 130, 16, 1]
+    seq_lens = [90, 33, 64, 12, 130, 200, 1]
+    case = workloads.make_case("vsmall", 300 + head_dim + hq + bs, q_lens, seq_lens, num_q_heads=hq,
+                               num_kv_heads=hkv, head_dim=head_dim, block_size=bs, dtype=dtype, causal=causal)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    out = run_varlen(case, kc, vc)
+    check_close(out, oracle_varlen(case, ko, vo), dtype, label=f"D{head_dim} G{hq // hkv} bs{bs} causal={causal}")
+
+
+def test_qlen1_batch_matches_decode():
+    case = workloads.decode_case("v1", 71, [5, 700, 33, 4000], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                 block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    a = run_varlen(case, kc, vc)
+    b = pa.paged_attention_decode(case.q.to(DEV), kc, vc, case.block_tables.to(DEV), case.seq_lens.to(DEV),
+                                  case.scale, num_splits=1)
+    diff = (a.float() - b.float()).abs().max().item()
+    assert diff <= 2e-2
+
+
+def test_chunked_prefill_matches_full_prefill():
+    """The last chunk of a prompt, run as a chunk over its prior context, equals those rows
+    of the full prompt's causal prefill."""
+    L, chunk = 700, 180
+    full = workloads.make_case("cf", 81, [L], [L], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(full)
+    out_full = run_varlen(full, kc, vc)
+    q_tail = full.q[L - chunk:].to(DEV)
+    qsl = torch.tensor([0, chunk], dtype=torch.int32, device=DEV)
+    out_chunk = pa.paged_attention_varlen(q_tail, kc, vc, qsl, full.seq_lens.to(DEV), full.block_tables.to(DEV),
+                                          chunk, True, full.scale)
+    diff = (out_chunk.float() - out_full[L - chunk:].float()).abs().max().item()
+    assert diff <= 2e-2
+
+
+def test_query_longer_than_context_is_flagged():
+    case = workloads.make_case("bad", 91, [4, 3], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    bad_lens = case.seq_lens.clone()
+    bad_lens[0] = 2                                   # q_len 4 > seq_len 2
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pa.paged_attention_varlen(case.q.to(DEV), kc, vc, case.query_start_loc.to(DEV), bad_lens.to(DEV),
+                                    case.block_tables.to(DEV), case.max_query_len, True, case.scale,
+                                    error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa._lib.PA_ERRBIT_QUERY_LAYOUT
+    assert torch.equal(out[:4].float(), torch.zeros_like(out[:4].float()))
+    ko, vo = oracle_pools(case)
+    want = oracle_varlen(case, ko, vo)
+    check_close(out[4:], want[4:], torch.bfloat16, label="clean request")
