@@ -66,7 +66,8 @@ typedef enum pa_dtype {
 
 /* Bits a kernel ORs into *error_word (see conventions above). */
 #define PA_ERRBIT_PAGE_OUT_OF_POOL   1  /* table entry outside [0, num_blocks): that page reads as zeros   */
-#define PA_ERRBIT_LENGTH_OUT_OF_RANGE 2 /* length < 0 or > max_blocks_per_seq*block_size: clamped          */
+#define PA_ERRBIT_LENGTH_OUT_OF_RANGE 2 /* length < 0 or > max_blocks_per_seq*block_size: decode clamps it,
+                                           varlen zeroes that request's rows                            */
 #define PA_ERRBIT_SLOT_OUT_OF_POOL   4  /* slot >= num_blocks*block_size or < -1: token not written         */
 #define PA_ERRBIT_QUERY_LAYOUT       8  /* query_start_loc not monotone or q_len > seq_len: rows zeroed     */
 #define PA_ERRBIT_WAIT_TIMEOUT      16  /* an internal bounded wait expired: that tile's output is invalid */
@@ -149,10 +150,14 @@ pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const vo
  * "TileInfer.jl - Attention kernels", Prefill and Walking the block table.
  *   q, out [num_tokens, Hq, D]; query_start_loc [R+1] int32 (query_start_loc[R] must equal
  *   num_tokens); seq_lens [R] int32; block_tables [R, max_blocks_per_seq] int32;
- *   max_query_len: host upper bound on any q_len (fixes the grid; longer blocks are flagged
- *   and their excess rows left unwritten... see PA_ERRBIT_QUERY_LAYOUT).
- * Supported: D in {64, 128, 256}; bf16 with Hq/Hkv in {1,2,4,8,16} (tensor-core path for
- *   D = 128 and block_size % 16 == 0), f32 with (Hq/Hkv) * D <= 2048. */
+ *   max_query_len: host upper bound on any q_len; it fixes the grid of the tensor-core path,
+ *   whose rows past it are left unwritten and flagged (PA_ERRBIT_QUERY_LAYOUT).
+ *   A request whose q_len exceeds its seq_len, or whose seq_len exceeds
+ *   max_blocks_per_seq * block_size, gets zero rows and a flag.
+ * Supported: D in {64, 128, 256}; bf16 with Hq/Hkv <= 16 and block_size % 16 == 0 (the
+ *   tcgen05 tensor-core kernel serves D = 128, Hq/Hkv in {1,2,4,8,16}, block_size in
+ *   {16,32,64,128}; other bf16 shapes run every query token as a one-split decode);
+ *   f32 with (Hq/Hkv) * D <= 2048 and any block_size. */
 pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const void* v_cache,
                                     const int32_t* query_start_loc, const int32_t* seq_lens,
                                     const int32_t* block_tables,

@@ -56,6 +56,9 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     if (unit < start || unit >= stop || q_len > seq) {
       if (report) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
       len = 0;
+    } else if (seq > p.max_blocks * p.block_size) {
+      if (report) flag_error(p.err, PA_ERRBIT_LENGTH_OUT_OF_RANGE);
+      len = 0;
     } else {
       const int pos = seq - q_len + (unit - start);  // queries are the newest positions
       len = p.causal ? pos + 1 : seq;
