@@ -167,6 +167,34 @@ pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const vo
                                     int causal, float scale, pa_dtype dtype,
                                     void* out, int32_t* error_word, void* stream);
 
+/* pa_paged_attention_decode_static_scratch: the same decode, for callers that cannot allocate.
+ * The pages describe no such variant; it exists for callers with no way to provide device
+ * scratch: a plugin that its host framework gives only input and output pointers (no allocator,
+ * no workspace hook), a runtime that has carved all device memory into its own pools and
+ * forbids cudaMalloc after start-up, or a latency-bound loop that cannot pay cudaMalloc's
+ * implicit device synchronisation.
+ *   Arguments, layouts, results and supported shapes are those of pa_paged_attention_decode
+ *   without `workspace` / `workspace_bytes`: the split partials go to a fixed 16 MiB
+ *   (16,777,216-byte) array compiled into the library, which every GPU that loads the library
+ *   holds until the process exits. The call allocates and frees nothing.
+ *   - A batch whose partials need more than 16 MiB (units * splits * Hq * (D + 2) * 4 bytes,
+ *     see pa_decode_workspace_bytes) is refused with PA_ERR_WORKSPACE_TOO_SMALL before
+ *     anything is enqueued; pass a smaller num_splits (1 needs no scratch at all).
+ *   - The first call on a device, with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ *     capture on that device. A failed lookup returns PA_ERR_CUDA.
+ *   - Every call on a device shares the one array and it keeps the previous call's contents.
+ *     Nothing in it needs to start at zero: each call writes every partial it later reads.
+ *     Two calls that overlap on the GPU (e.g. on different streams) race on the array and give
+ *     undefined results; serialise them. */
+pa_status pa_paged_attention_decode_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                                   const int32_t* block_tables, const int32_t* context_lens,
+                                                   int num_seqs, int num_q_heads, int num_kv_heads,
+                                                   int head_dim, int block_size, int num_blocks,
+                                                   int max_blocks_per_seq, float scale, pa_dtype dtype,
+                                                   int num_splits, void* out, int32_t* error_word,
+                                                   void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -38,6 +38,8 @@ SIGNATURES = {
                                        _p, _p, _sz, _p, _p]),
     "pa_paged_attention_varlen": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                        _i, _f, _i, _p, _p, _p]),
+    "pa_paged_attention_decode_static_scratch": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f,
+                                                      _i, _i, _p, _p, _p]),
 }
 
 _lib = None
