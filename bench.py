@@ -255,6 +255,10 @@ def decode_leg(args, world, rank, dev):
     import paged_kv_attention_gb300 as pa
     import workloads
     case = workloads.NAMED[DECODE_WORKLOAD]()
+    if args.decode_seqs != case.num_reqs:  # a smaller batch of the same workload (profiling)
+        case = workloads.decode_case(f"decode_{args.decode_seqs}x4096_bf16", 1003, [4096] * args.decode_seqs,
+                                     num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                     dtype=torch.bfloat16)
     S, Hq, Hkv, D, bs = case.num_reqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
     lens = case.seq_lens.tolist()
     kc, vc = (t.to(dev) for t in case.empty_pools())
@@ -307,6 +311,10 @@ def decode_leg(args, world, rank, dev):
     step_bytes = call_bytes + cache_write_bytes(S, Hkv, D, 2)
     value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
 
+    if args.no_e2e:
+        return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
+                    call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=None, h2d=0, d2h=0,
+                    launches=args.steps * (2 + (1 if splits > 1 else 0)))
     # end to end: host buffers in, host result out, inside the timed region
     hq = q.cpu().pin_memory()
     hk, hv, hs, hl = (t.pin_memory() for t in (new_k, new_v, new_slots, case.seq_lens))
@@ -341,6 +349,10 @@ def prefill_leg(args, dev, steps):
     import paged_kv_attention_gb300 as pa
     import workloads
     case = workloads.NAMED[PREFILL_WORKLOAD]()
+    if args.prefill_seqs != case.num_reqs:  # a smaller batch of the same workload (profiling)
+        case = workloads.make_case(f"prefill_{args.prefill_seqs}x8192_bf16", 1005, [8192] * args.prefill_seqs,
+                                   [8192] * args.prefill_seqs, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                   block_size=64, dtype=torch.bfloat16)
     kc, vc = (t.to(dev) for t in case.empty_pools())
     q = case.q.to(dev)
     key, value, slots = case.key.to(dev), case.value.to(dev), case.slot_mapping.to(dev)
@@ -381,6 +393,11 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="run one leg only (profiling runs)")
+    ap.add_argument("--decode-seqs", type=int, default=64, help="sequences of 4096 tokens in the decode leg")
+    ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -396,9 +413,14 @@ def main():
     traffic = load_traffic()
 
     with ClockSampler(local) as clocks:
-        d = decode_leg(args, world, rank, dev)
-        p = None if args.no_prefill else prefill_leg(args, dev, args.prefill_steps)
+        d = None if args.only == "prefill" else decode_leg(args, world, rank, dev)
+        p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps)
     clk = clocks.summary()
+    if d is None:
+        if rank == 0 and p is not None:
+            print(json.dumps({"prefill_only": True, "workload": p["case"].name, "value": round(p["tflops"], 2),
+                              "unit": "TFLOP/s", "attn_ms": round(p["attn_ms"], 4), "clocks": clk}), flush=True)
+        return
 
     case = d["case"]
     dec_achieved = d["call_bytes"] / (d["call_ms"] / 1e3) / 1e9
@@ -416,7 +438,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": DECODE_WORKLOAD, "num_seqs": case.num_reqs, "context_len": 4096,
+        "config": {"workload": case.name, "num_seqs": case.num_reqs, "context_len": 4096,
                    "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
                    "block_size": case.block_size, "num_splits": d["splits"],
                    "step": "reshape_and_cache(64 new rows) + decode(split-KV + combine)",
@@ -429,8 +451,9 @@ def main():
                      "algorithmic_bytes_per_launch": d["call_bytes"], "launch_ms": round(d["call_ms"], 5),
                      "traffic": traffic.get("decode_bf16_kernel")},
         "cache_write_ms": round(d["write_ms"], 5),
-        "e2e": {"value": round(d["e2e_value"], 2), "unit": "GB/s", "h2d_bytes_per_step": d["h2d"],
-                "d2h_bytes_per_step": d["d2h"]},
+        "e2e": None if d["e2e_value"] is None else {
+            "value": round(d["e2e_value"], 2), "unit": "GB/s", "h2d_bytes_per_step": d["h2d"],
+            "d2h_bytes_per_step": d["d2h"]},
         "gpu_launches": d["launches"],
         "clocks": clk,
     }
@@ -444,7 +467,7 @@ def main():
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": round(p["tflops"] / tf_peak, 4),
                          "peak_source": peak_src, "traffic": traffic.get("varlen_kernel")},
         }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and case.num_reqs == 64:
         _, ko_vo = None, oracle_pools(case)
         v, dt, n, threads = time_oracle_decode(case, *ko_vo)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
