@@ -344,7 +344,7 @@ extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cach
     vp.max_blocks = max_blocks_per_seq;
     vp.max_query_len = max_query_len;
     const int tokens_per_tile = 128 / G;
-    vp.q_tiles = (int)cdivll(max_query_len, tokens_per_tile);
+    vp.q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
     vp.causal = causal ? 1 : 0;
     vp.scale_log2 = sc * kLog2e;
     CUtensorMap qmap, kmap, vmap;

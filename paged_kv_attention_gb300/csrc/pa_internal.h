@@ -76,11 +76,12 @@ struct VarlenParams {
   int num_blocks;
   int max_blocks;
   int max_query_len;
-  int q_tiles;  // cdiv(max_query_len, tokens per tile)
+  int q_tiles;  // cdiv(max_query_len, tokens per CTA)
   int causal;
   float scale_log2;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
+int varlen_tc_tokens_per_cta(int group);
 cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream);
 

@@ -2,27 +2,28 @@
 //
 // Method ("32. Production attention kernels", One kernel for the whole batch;
 // "TileInfer.jl - Attention kernels", Prefill and Walking the block table):
-//  * one CTA per (query tile, request, KV head). A query tile is 128 packed rows: 128/G
-//    consecutive query tokens of the request times the G query heads of the KV head
-//    (row m = token m / G, head m % G), so each K/V tile serves the whole group;
+//  * a query tile is 128 packed rows: 128/G consecutive query tokens of one request times
+//    the G query heads of one KV head (row m = token m / G, head m % G), so every K/V tile
+//    serves the whole group;
 //  * request r's q_len queries are the newest of its seq_len positions (query t sits at
 //    seq_len - q_len + t) and see keys up to their own position; the key loop stops at the
 //    tile's last query and only tiles that cross the diagonal or the sequence end are masked;
 //  * FlashAttention-2 online softmax in fp32 with exp2 (scale pre-multiplied by log2 e);
 //    probabilities are rounded to bf16 for the P.V product.
 //
-// GB300 mapping:
-//  * warp 4 (one lane) walks the block table and issues TMA loads: the Q tile once, then a
-//    two-stage ring of 128-key K and V tiles, one box per page per 64-column half, in the
-//    128-byte-swizzled layout the tensor core reads directly;
-//  * warp 5 owns the tensor memory (512 columns: two 128-column score buffers and the
-//    128-column output accumulator) and one lane issues tcgen05.mma: S = Q K^T (M=128,
-//    N=128, K=128) into the free score buffer while the softmax works on the other, then
-//    O += P V (two N=64 halves) once the softmax has written P;
-//  * warps 0-3 (one thread per row) read S from TMEM, mask, update the running max/sum,
-//    write P (bf16, swizzled) to shared memory and rescale O in TMEM only when the running
-//    max rose by more than 2^8 (the result is exact for any reference max; this only
-//    bounds the fp32 range of P and O);
+// GB300 mapping. One CTA owns two consecutive query tiles (A, B) of one (request, KV head)
+// and streams the K/V tiles they need once for both:
+//  * warp 8 (one lane) walks the block table and issues TMA loads: both Q tiles once, then
+//    two-stage rings for K and V (128-key tiles, one box per page per 64-column half,
+//    128-byte swizzle, the layout the tensor core reads directly);
+//  * warp 9 owns the tensor memory (512 columns: S_A, S_B, O_A, O_B, 128 each) and one lane
+//    issues tcgen05.mma in the order S_A(j), S_B(j), PV_A(j), S_A(j+1), PV_B(j), S_B(j+1),
+//    ... so that the tensor core works on one tile while the other tile's softmax runs;
+//  * warps 0-3 (tile A) and 4-7 (tile B), one thread per row, read S from TMEM, mask, update
+//    the running max/sum, write P as bf16 back into the first 64 columns of their S block
+//    and signal; P.V then takes its A operand from TMEM (no shared-memory round trip for P).
+//    O is rescaled in TMEM only when the running max rose by more than 2^8 (exact for any
+//    reference max; this only bounds the range of P and O);
 //  * every wait is bounded; on expiry the CTA flags PA_ERRBIT_WAIT_TIMEOUT, drains its
 //    outstanding copies and MMAs, frees its tensor memory and exits.
 #include "pa_common.cuh"
@@ -35,18 +36,30 @@ constexpr int kBM = 128;  // packed query rows per tile
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kD = 128;   // head dim of this kernel
 constexpr int kStages = 2;
-constexpr int kRegion = 128 * 128;      // one [128 rows][64 bf16] swizzled column half: 16 KiB
-constexpr int kTileBytes = 2 * kRegion; // a 128 x 128 bf16 tile
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kRegion = 128 * 128;       // one [128 rows][64 bf16] swizzled column half: 16 KiB
+constexpr int kTileBytes = 2 * kRegion;  // a 128 x 128 bf16 tile
+constexpr int kOffQ = 0;                 // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
-enum { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_P = 9, B_O = 10, B_FIN = 11, kNumBars = 12 };
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+enum {
+  B_Q = 0,
+  B_KF = 1,   // +stage
+  B_VF = 3,   // +stage
+  B_KE = 5,   // +stage
+  B_VE = 7,   // +stage
+  B_SF = 9,   // +tile (A, B)
+  B_PR = 11,  // +tile
+  B_OD = 13,  // +tile
+  B_FIN = 15,
+  kNumBars = 16
+};
 constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 32;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+// TMEM columns of tile t's score block and output accumulator
+__host__ __device__ constexpr uint32_t col_s(int t) { return t == 0 ? 0u : 128u; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return t == 0 ? 256u : 384u; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // ---------------------------------------------------------------- tcgen05 helpers
@@ -68,11 +81,21 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D(tmem) (+)= A(smem) * B(smem)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// D(tmem) (+)= A(tmem) * B(smem); A is M rows on the TMEM lanes, two bf16 per column.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -114,15 +137,46 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted. The clock and the
+// abort flag are checked once per 64 polls so that waiting warps take few issue slots.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// ---------------------------------------------------------------- softmax arithmetic
+// 2^x on the special-function unit (flushes results below 2^-126 to zero: such
+// probabilities are far below bf16 resolution against the row maximum's 1).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Packed fp32 pairs (Blackwell f32x2 arithmetic: one instruction for two lanes of work).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // The same, with one verdict for the whole warp, so that a warp either proceeds to its
@@ -137,6 +191,21 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag, int32_t* err
   flag_error(err, PA_ERRBIT_WAIT_TIMEOUT);
 }
 
+struct TileSpan {
+  int n_tok;    // valid query tokens in the tile (0 = tile unused)
+  int first;    // position of the tile's first query
+  int n_kv;     // 128-key tiles it needs
+};
+
+__device__ __forceinline__ TileSpan tile_span(int tok0, int TOK, int q_len, int seq_len, int causal) {
+  TileSpan t;
+  t.n_tok = max(0, min(TOK, q_len - tok0));
+  t.first = seq_len - q_len + tok0;
+  const int key_end = causal ? min(seq_len, t.first + t.n_tok) : seq_len;
+  t.n_kv = t.n_tok > 0 ? (key_end + kBN - 1) / kBN : 0;
+  return t;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_tc_kernel(const __grid_constant__ VarlenParams p, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
@@ -147,14 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* issued_tiles = reinterpret_cast<int*>(tmem_slot + 2);
 
-  // ---- which tile: heaviest (last) query tiles first across all requests and heads
+  // ---- which tile pair: heaviest (last) query tiles first across all requests and heads
   const int per_tile = p.num_reqs * p.num_kv_heads;
   const int tile = p.q_tiles - 1 - (int)(blockIdx.x / per_tile);
   const int rem = (int)(blockIdx.x % per_tile);
   const int r = rem / p.num_kv_heads;
   const int kvh = rem - r * p.num_kv_heads;
   const int G = p.group;
-  const int TOK = kBM / G;
+  const int TOK = kBM / G;  // tokens per 128-row tile; a CTA covers 2 * TOK tokens
   const int tid = threadIdx.x;
 
   const int q_start = p.query_start_loc[r];
@@ -164,16 +233,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool layout_ok = q_start >= 0 && q_len >= 0 && q_stop <= p.num_tokens;
   const bool too_long = seq_len > p.max_blocks * p.block_size;
   const bool bad = !layout_ok || q_len > seq_len || too_long;
+  const int tok0 = tile * 2 * TOK;
   if (bad) {
     if (tid == 0 && kvh == 0 && tile == 0)
       flag_error(p.err, too_long && layout_ok && q_len <= seq_len ? PA_ERRBIT_LENGTH_OUT_OF_RANGE
                                                                    : PA_ERRBIT_QUERY_LAYOUT);
-    if (!layout_ok) return;
+    if (!layout_ok || tok0 >= q_len) return;
     // a request the kernel cannot serve gives zero rows
-    const int tok0 = tile * TOK;
-    if (tok0 >= q_len) return;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-    const int rows = min(TOK, q_len - tok0) * G;
+    const int rows = min(2 * TOK, q_len - tok0) * G;
     for (int i = tid; i < rows * (kD / 8); i += blockDim.x) {
       const int row = i / (kD / 8), c = i % (kD / 8);
       const size_t o = ((size_t)(q_start + tok0 + row / G) * p.num_q_heads + kvh * G + row % G) * kD + c * 8;
@@ -182,13 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   if (tile == 0 && kvh == 0 && tid == 0 && q_len > p.max_query_len) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
-  const int tok0 = tile * TOK;
-  if (tok0 >= q_len) return;  // nothing of this request in this tile (uniform: whole CTA leaves)
+  if (tok0 >= q_len) return;  // nothing of this request here (uniform: the whole CTA leaves)
 
-  const int n_tok = min(TOK, q_len - tok0);
-  const int first_pos = seq_len - q_len + tok0;
-  const int key_end = p.causal ? min(seq_len, first_pos + n_tok) : seq_len;  // keys [0, key_end)
-  const int n_kv = (key_end + kBN - 1) / kBN;
+  const TileSpan spanA = tile_span(tok0, TOK, q_len, seq_len, p.causal);
+  const TileSpan spanB = tile_span(tok0 + TOK, TOK, q_len, seq_len, p.causal);
+  const int n_kv = max(spanA.n_kv, spanB.n_kv);
   const int bs = p.block_size;
   const int pages_per_tile = kBN / bs;
   const int seq_pages = (seq_len + bs - 1) / bs;
@@ -199,17 +265,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[B_KF + s], 1);
       mbar_init(&bars[B_VF + s], 1);
-      mbar_init(&bars[B_KVE + s], 1);
-      mbar_init(&bars[B_SF + s], 1);
+      mbar_init(&bars[B_KE + s], 1);
+      mbar_init(&bars[B_VE + s], 1);
     }
-    mbar_init(&bars[B_P], kBM);
-    mbar_init(&bars[B_O], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[B_SF + t], 1);
+      mbar_init(&bars[B_PR + t], kBM);
+      mbar_init(&bars[B_OD + t], 1);
+    }
     mbar_init(&bars[B_FIN], 1);
     fence_barrier_init();
     *abort_flag = 0;
     *issued_tiles = 0;
   }
-  if (warp == 5) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
@@ -220,30 +289,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t sQ = smem_addr(smem + kOffQ);
-  const uint32_t sK = smem_addr(smem + kOffK);
-  const uint32_t sV = smem_addr(smem + kOffV);
-  const uint32_t sP = smem_addr(smem + kOffP);
-
-  if (warp == 4) {
-    // ------------------------------------------------ producer: Q once, then K/V tiles
+  if (warp == 8) {
+    // ------------------------------------------------ producer: Q_A, Q_B once, then K/V tiles
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      mbar_arrive_expect_tx(&bars[B_Q], kTileBytes);
-      for (int a = 0; a < 2; ++a)
-        tma_load_3d(smem + kOffQ + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G, q_start + tok0);
+      mbar_arrive_expect_tx(&bars[B_Q], 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int a = 0; a < 2; ++a)
+          tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
+                      q_start + tok0 + t * TOK);
       const int32_t* table = p.block_tables + (size_t)r * p.max_blocks;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kStages;
-        if (j >= kStages && !wait_or_abort(&bars[B_KVE + st], ((j / kStages) - 1) & 1, abort_flag)) {
-          set_abort(abort_flag, p.err);
-          break;
-        }
+        const uint32_t round_parity = ((j / kStages) - 1) & 1;
         const int p0 = j * pages_per_tile;
         const int p1 = min(p0 + pages_per_tile, seq_pages);
         const uint32_t bytes = (uint32_t)(p1 - p0) * bs * 256u;
+        if (j >= kStages && !wait_or_abort(&bars[B_KE + st], round_parity, abort_flag)) {
+          set_abort(abort_flag, p.err);
+          break;
+        }
         mbar_arrive_expect_tx(&bars[B_KF + st], bytes);
         for (int pg = p0; pg < p1; ++pg) {
           const int page = table[pg];
@@ -251,6 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int a = 0; a < 2; ++a)
             tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + (pg - p0) * bs * 128, &kmap,
                         &bars[B_KF + st], a * 64, kvh, 0, page);
+        }
+        if (j >= kStages && !wait_or_abort(&bars[B_VE + st], round_parity, abort_flag)) {
+          set_abort(abort_flag, p.err);
+          *issued_tiles = j + 1;  // K of tile j is in flight
+          break;
         }
         mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
         for (int pg = p0; pg < p1; ++pg) {
@@ -262,97 +334,137 @@ __global__ void __launch_bounds__(kThreads, 1)
         *issued_tiles = j + 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer (lane 0); the warp zeroes V tails
     const uint32_t id_s = idesc_bf16(kBM, kBN, false);
     const uint32_t id_pv = idesc_bf16(kBM, 64, true);
-    bool ok = warp_wait(&bars[B_Q], 0, abort_flag);
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % kStages;
-      if (!warp_wait(&bars[B_KF + st], (j / kStages) & 1, abort_flag)) return false;
-      tc_fence_after();
+    const uint32_t sQ = smem_addr(smem + kOffQ);
+    const uint32_t sK = smem_addr(smem + kOffK);
+    const uint32_t sV = smem_addr(smem + kOffV);
+    const int nA = spanA.n_kv, nB = spanB.n_kv;
+    // S_t(j) = Q_t K_j^T into S block t
+    auto issue_s = [&](int t, int j) {
       if (lane == 0) {
-        const uint32_t d = tmem + (uint32_t)((j & 1) * kBN);
-        const uint32_t kb = sK + st * kTileBytes;
-#pragma unroll
+        const uint32_t qb = sQ + t * kTileBytes;
+        const uint32_t kb = sK + (j % kStages) * kTileBytes;
+#pragma unroll 1
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-          umma_bf16(d, sdesc(sQ + off, 16, 1024), sdesc(kb + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + col_s(t), sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars[B_SF + (j & 1)]);
+        umma_commit(&bars[B_SF + t]);
       }
-      __syncwarp();
-      return true;
     };
-    if (ok) ok = issue_s(0);
+    // O_t += P_t(j) V_j, P_t from the first 64 TMEM columns of S block t
+    auto issue_pv = [&](int t, int j) {
+      if (lane == 0) {
+        const uint32_t vb = sV + (j % kStages) * kTileBytes;
+#pragma unroll 1
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            umma_ts(tmem + col_o(t) + 64 * h, tmem + col_s(t) + 8 * kk,
+                    sdesc(vb + h * kRegion + kk * 2048, 1024, 1024), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars[B_OD + t]);
+      }
+    };
+    auto commit_if = [&](bool cond, int bar) {
+      if (cond && lane == 0) umma_commit(&bars[bar]);
+    };
+    bool ok = warp_wait(&bars[B_Q], 0, abort_flag) && warp_wait(&bars[B_KF], 0, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      if (nA > 0) issue_s(0, 0);
+      if (nB > 0) issue_s(1, 0);
+      commit_if(kStages < n_kv, B_KE + 0);
+      __syncwarp();
+    }
     for (int j = 0; ok && j < n_kv; ++j) {
-      if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-      if (!(ok = warp_wait(&bars[B_P], j & 1, abort_flag))) break;
       const int st = j % kStages;
       if (!(ok = warp_wait(&bars[B_VF + st], (j / kStages) & 1, abort_flag))) break;
       const int zero_from = seq_len - j * kBN;  // V rows at or past the sequence end: exact zeros
       if (zero_from < kBN) {
-        uint8_t* vb = smem + kOffV + st * kTileBytes;
+        uint8_t* vbp = smem + kOffV + st * kTileBytes;
         const int rows = kBN - zero_from;
         for (int i = lane; i < rows * 16; i += 32) {
           const int row = zero_from + i / 16, c = i % 16;
-          *reinterpret_cast<uint4*>(vb + (c >> 3) * kRegion + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vbp + (c >> 3) * kRegion + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();
         __syncwarp();
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t vb = sV + st * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t a = sdesc(sP + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            umma_bf16(tmem + kColO + 64 * h, a, sdesc(vb + h * kRegion + kk * 2048, 1024, 1024), id_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        // release the stage only when the producer will refill it: an arrive that nobody
-        // waits for could land after this CTA has left
-        if (j + kStages < n_kv) umma_commit(&bars[B_KVE + st]);
-        umma_commit(&bars[B_O]);
+      if (j < nA) {
+        if (!(ok = warp_wait(&bars[B_PR + 0], j & 1, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(0, j);
+      }
+      const bool next = j + 1 < n_kv;
+      if (next) {
+        if (!(ok = warp_wait(&bars[B_KF + (j + 1) % kStages], ((j + 1) / kStages) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (j + 1 < nA) issue_s(0, j + 1);
+      }
+      if (j < nB) {
+        if (!(ok = warp_wait(&bars[B_PR + 1], j & 1, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(1, j);
+      }
+      // release V_j, then issue S_B(j+1) and release K_{j+1}, each only if the producer will
+      // refill that stage (an arrive nobody waits for could land after this CTA has left)
+      commit_if(j + kStages < n_kv, B_VE + st);
+      if (next) {
+        if (j + 1 < nB) issue_s(1, j + 1);
+        commit_if(j + 1 + kStages < n_kv, B_KE + (j + 1) % kStages);
       }
       __syncwarp();
     }
     if (!ok) set_abort(abort_flag, p.err);
   } else {
-    // ------------------------------------------------ softmax: one thread per packed row
-    const int row = tid;
-    const int t = tok0 + row / G;
-    const bool row_valid = t < q_len;
-    const int qpos = seq_len - q_len + t;
+    // ------------------------------------------------ softmax: warps 0-3 tile A, 4-7 tile B
+    const int t = warp >> 2;
+    const TileSpan span = t == 0 ? spanA : spanB;
+    const int row = tid & (kBM - 1);
+    const int tok = tok0 + t * TOK + row / G;
+    const bool row_valid = tok < q_len;
+    const int qpos = seq_len - q_len + tok;
     const int vis_end = p.causal ? min(qpos + 1, seq_len) : seq_len;
     const float c = p.scale_log2;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = lane_base + col_s(t);
+    const uint32_t o_col = lane_base + col_o(t);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    uint8_t* prow = smem + kOffP + row * 128;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!warp_wait(&bars[B_SF + (j & 1)], (j >> 1) & 1, abort_flag)) {
+    for (int j = 0; j < span.n_kv; ++j) {
+      if (!warp_wait(&bars[B_SF + t], j & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const int nvis = vis_end - j * kBN;  // keys of this tile the row may see
+      const bool full = nvis >= kBN;
+      // the row's 128 scores, one TMEM round trip (tcgen05.wait::ld waits for every load)
       uint32_t sv[4][32];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(lane_base + (uint32_t)((j & 1) * kBN + 32 * q4), sv[q4]);
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_col + 32 * q4, sv[q4]);
       tmem_ld_wait();
-      const int nvis = vis_end - j * kBN;
-      float mx = -INFINITY;
+      if (!full) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)  // select: NaN past the sequence end never survives
+            sv[q4][i] = (q4 * 32 + i < nvis) ? sv[q4][i] : __float_as_uint(-INFINITY);
+      }
+      // row maximum over eight interleaved chains (short dependency chains)
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x = __uint_as_float(sv[q4][i]);
-          x = (q4 * 32 + i < nvis) ? x : -INFINITY;  // select: NaN past the end never survives
-          sv[q4][i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+        for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[q4][i]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mxs = mx * c;
       float m_new = m_run, alpha = 1.f;
       bool rescale = false;
@@ -362,60 +474,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = (j > 0);
       }
       const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-      float lsum = 0.f;
-      uint32_t pk[64];
+      // probabilities, packed to bf16 pairs over the score columns already consumed
+      // (keys 64h..64h+63 -> columns 32h..32h+31)
+      const uint64_t c2 = f2(c, c), nmu2 = f2(-mu, -mu);
+      uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sv[q4][i]), c, -mu));
-          const float p1 = exp2f(fmaf(__uint_as_float(sv[q4][i + 1]), c, -mu));
-          lsum += p0 + p1;
-          pk[q4 * 16 + i / 2] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t* src = sv[2 * h + (i >> 4)];
+          const int e = (2 * i) & 31;
+          float x0, x1;
+          f2_split(f2_fma(f2(__uint_as_float(src[e]), __uint_as_float(src[e + 1])), c2, nmu2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);  // 2^-inf = 0 for masked keys
+          sum2[i & 1] = f2_add(sum2[i & 1], f2(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);  // key 64h + 2i in the low half, 64h + 2i + 1 in the high half
         }
+        tmem_st32(s_col + 32 * h, pk);
+      }
+      float la, lb;
+      f2_split(f2_add(sum2[0], sum2[1]), la, lb);
+      const float lsum = la + lb;
       l_run = l_run * alpha + lsum;
       m_run = m_new;
-      // P and O belong to the previous P.V until it completes
-      if (j > 0 && !warp_wait(&bars[B_O], (j - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int region = u >> 3, unit = u & 7;
-        *reinterpret_cast<uint4*>(prow + region * kRegion + ((unit ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      }
+      // S_t(j) has landed, so P.V of tile j-1 (issued before it) is complete: O is stable
       if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? alpha : 1.f;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t ov[32];
-          tmem_ld32(lane_base + kColO + 32 * q4, ov);
+          tmem_ld32(o_col + 32 * q4, ov);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-          tmem_st32(lane_base + kColO + 32 * q4, ov);
+          tmem_st32(o_col + 32 * q4, ov);
         }
-        tmem_st_wait();
       }
-      fence_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[B_P]);
+      mbar_arrive(&bars[B_PR + t]);
     }
-    if (ok && !warp_wait(&bars[B_O], (n_kv - 1) & 1, abort_flag)) ok = false;
+    if (ok && span.n_kv > 0 && !warp_wait(&bars[B_OD + t], (span.n_kv - 1) & 1, abort_flag)) ok = false;
     if (!ok) {
       set_abort(abort_flag, p.err);
-    } else {
+    } else if (span.n_kv > 0) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                           ((size_t)(q_start + t) * p.num_q_heads + kvh * G + row % G) * kD;
+                           ((size_t)(q_start + tok) * p.num_q_heads + kvh * G + row % G) * kD;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t ov[32];
-        tmem_ld32(lane_base + kColO + 32 * q4, ov);
+        tmem_ld32(o_col + 32 * q4, ov);
         tmem_ld_wait();
         if (row_valid) {
 #pragma unroll
@@ -436,11 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (*abort_flag) {
     // drain: every MMA this CTA issued, every copy still landing
-    if (warp == 5 && lane == 0) {
+    if (warp == 9 && lane == 0) {
       umma_commit(&bars[B_FIN]);
       (void)mbar_wait(&bars[B_FIN], 0);
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
       (void)mbar_wait(&bars[B_Q], 0);
       const int issued = *issued_tiles;
       for (int j = max(0, issued - kStages); j < issued; ++j) {
@@ -450,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
@@ -463,6 +574,8 @@ bool varlen_tc_supported(int head_dim, int group, int block_size) {
   const bool bs_ok = block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128;
   return head_dim == kD && g_ok && bs_ok;
 }
+
+int varlen_tc_tokens_per_cta(int group) { return 2 * (kBM / group); }
 
 cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {
