@@ -85,26 +85,32 @@ def load_peaks():
 
 
 def load_traffic():
-    """Per-launch DRAM bytes of the dominant kernels from the committed ncu summary, when the
-    kernels have not changed since (the summary records the source hash it was taken at)."""
+    """Per-launch DRAM bytes of the dominant kernels from the committed ncu summaries, for each
+    kernel whose source file is unchanged since the capture (its hash is recorded)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return {}
-    if d.get("source_hash") != source_hash():
-        return {}
-    return d.get("per_launch_bytes", {})
+    out = {}
+    for name, k in d.get("kernels", {}).items():
+        if k.get("source_hash") == source_hash(k.get("source", "")):
+            out[name] = k.get("bytes_per_launch")
+    return out
 
 
-def source_hash() -> str:
+def source_hash(source: str) -> str:
+    """Hash of one kernel source file plus the shared device header it includes."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for name in (source, "pa_common.cuh"):
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+        except OSError:
+            return ""
     return h.hexdigest()[:16]
 
 

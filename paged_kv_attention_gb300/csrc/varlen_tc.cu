@@ -17,7 +17,8 @@
 //    two-stage rings for K and V (128-key tiles, one box per page per 64-column half,
 //    128-byte swizzle, the layout the tensor core reads directly);
 //  * warp 9 owns the tensor memory (512 columns: S_A, S_B, O_A, O_B, 128 each) and one lane
-//    issues tcgen05.mma in the order S_A(j), S_B(j), PV_A(j), S_A(j+1), PV_B(j), S_B(j+1),
+//    issues tcgen05.mma (S: M=128 N=128 K=128 from shared memory; P.V: M=128 N=128 K=128
+//    with A from TMEM) in the order S_A(j), S_B(j), PV_A(j), S_A(j+1), PV_B(j), S_B(j+1),
 //    ... so that the tensor core works on one tile while the other tile's softmax runs;
 //  * warps 0-3 (tile A) and 4-7 (tile B), one thread per row, read S from TMEM, mask, update
 //    the running max/sum, write P as bf16 back into the first 64 columns of their S block
@@ -337,35 +338,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer (lane 0); the warp zeroes V tails
     const uint32_t id_s = idesc_bf16(kBM, kBN, false);
-    const uint32_t id_pv = idesc_bf16(kBM, 64, true);
+    const uint32_t id_pv = idesc_bf16(kBM, kD, true);
     const uint32_t sQ = smem_addr(smem + kOffQ);
     const uint32_t sK = smem_addr(smem + kOffK);
     const uint32_t sV = smem_addr(smem + kOffV);
     const int nA = spanA.n_kv, nB = spanB.n_kv;
+    // Descriptors advance by adding (byte offset >> 4) to the start-address field; every
+    // operand lies below 256 KiB of the shared window, so the 14-bit field never carries.
+    const uint64_t dq0 = sdesc(sQ, 16, 1024);
+    const uint64_t dk0 = sdesc(sK, 16, 1024);
+    const uint64_t dv0 = sdesc(sV, kRegion, 1024);  // MN-major V: 64-column halves kRegion apart
     // S_t(j) = Q_t K_j^T into S block t
     auto issue_s = [&](int t, int j) {
       if (lane == 0) {
-        const uint32_t qb = sQ + t * kTileBytes;
-        const uint32_t kb = sK + (j % kStages) * kTileBytes;
-#pragma unroll 1
+        const uint64_t dq = dq0 + (uint64_t)((t * kTileBytes) >> 4);
+        const uint64_t dk = dk0 + (uint64_t)(((j % kStages) * kTileBytes) >> 4);
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-          umma_ss(tmem + col_s(t), sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+          umma_ss(tmem + col_s(t), dq + off, dk + off, id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars[B_SF + t]);
       }
     };
-    // O_t += P_t(j) V_j, P_t from the first 64 TMEM columns of S block t
+    // O_t += P_t(j) V_j (N = 128: both 64-column halves of V), P_t from the first 64 TMEM
+    // columns of S block t
     auto issue_pv = [&](int t, int j) {
       if (lane == 0) {
-        const uint32_t vb = sV + (j % kStages) * kTileBytes;
-#pragma unroll 1
-        for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint64_t dv = dv0 + (uint64_t)(((j % kStages) * kTileBytes) >> 4);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            umma_ts(tmem + col_o(t) + 64 * h, tmem + col_s(t) + 8 * kk,
-                    sdesc(vb + h * kRegion + kk * 2048, 1024, 1024), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), id_pv,
+                  kk > 0 ? 1u : acc0);
         umma_commit(&bars[B_OD + t]);
       }
     };

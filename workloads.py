@@ -164,7 +164,8 @@ def decode_64x4096_bf16(head_dim: int = 128) -> PagedCase:
     16,384 pages needed, permuted. head_dim 128: 32 q / 8 KV heads; head_dim 256:
     16 q / 4 KV heads (the same 1,073,741,824 bytes of K+V)."""
     hq, hkv = (32, 8) if head_dim == 128 else (16, 4)
-    return decode_case(f"decode_64x4096_bf16_d{head_dim}", 1003 if head_dim == 128 else 1013,
+    name = "decode_64x4096_bf16" if head_dim == 128 else f"decode_64x4096_bf16_d{head_dim}"
+    return decode_case(name, 1003 if head_dim == 128 else 1013,
                        [4096] * 64, num_q_heads=hq, num_kv_heads=hkv, head_dim=head_dim,
                        block_size=16, dtype=torch.bfloat16)
 
