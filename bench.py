@@ -187,11 +187,19 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: every rank's work is counted against it."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_step_per_rank: float, steps: int, max_ms: float, world: int) -> float:
+    """Units per second over all ranks: every rank processes its own batch (weak scaling),
+    timed by the slowest rank."""
+    return world * units_per_step_per_rank * steps / (max_ms / 1e3)
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -290,6 +298,29 @@ def decode_leg(args, world, rank, dev):
     for _ in range(args.warmup):
         step(q, nk, nv, ns, ctx, out)
     torch.cuda.synchronize()
+
+    def write_call():
+        pa.reshape_and_cache(nk, nv, kc, vc, ns)
+
+    def decode_call():
+        pa.paged_attention_decode(q, kc, vc, tables, ctx, case.scale, num_splits=splits, out=out, workspace=ws)
+
+    if args.no_graph:
+        run_write, run_call = write_call, decode_call
+    else:
+        # the step's two calls, each captured once and replayed (launch shapes depend only on
+        # host sizes; lengths and positions are read from device buffers at every replay)
+        graphs = []
+        for fn in (write_call, decode_call):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs.append(g)
+        run_write, run_call = graphs[0].replay, graphs[1].replay
+        for _ in range(3):
+            run_write()
+            run_call()
+        torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
@@ -300,9 +331,9 @@ def decode_leg(args, world, rank, dev):
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        pa.reshape_and_cache(nk, nv, kc, vc, ns)
+        run_write()
         ev[i][1].record(stream)
-        pa.paged_attention_decode(q, kc, vc, tables, ctx, case.scale, num_splits=splits, out=out, workspace=ws)
+        run_call()
         ev[i][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -315,7 +346,7 @@ def decode_leg(args, world, rank, dev):
 
     call_bytes = decode_call_bytes(lens, Hq, Hkv, D, bs, 2)
     step_bytes = call_bytes + cache_write_bytes(S, Hkv, D, 2)
-    value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = whole_job_rate(step_bytes, args.steps, total_ms, world) / 1e9
 
     if args.no_e2e:
         return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
@@ -345,7 +376,7 @@ def decode_leg(args, world, rank, dev):
     e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end), world)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl))
     d2h = hout.numel() * hout.element_size()
-    e2e_value = world * step_bytes * args.steps / (e2e_ms / 1e3) / 1e9
+    e2e_value = whole_job_rate(step_bytes, args.steps, e2e_ms, world) / 1e9
     return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
                 call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=e2e_value, h2d=h2d, d2h=d2h,
                 launches=args.steps * (2 + (1 if splits > 1 else 0)))
@@ -404,6 +435,7 @@ def main():
     ap.add_argument("--decode-seqs", type=int, default=64, help="sequences of 4096 tokens in the decode leg")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the decode step eagerly, not as CUDA graphs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -448,6 +480,7 @@ def main():
                    "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
                    "block_size": case.block_size, "num_splits": d["splits"],
                    "step": "reshape_and_cache(64 new rows) + decode(split-KV + combine)",
+                   "launch": "eager" if args.no_graph else "CUDA graphs (one per call), replayed each step",
                    "l2": "no flush: 1.07 GB of K/V per step > 129 MB L2",
                    "parallelism": "replicas" if world == 1 else f"dp{world} (independent batches per GPU)"},
         "hbm_frac_of_peak": round(d["value"] / world / hbm, 4),
