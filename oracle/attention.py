@@ -91,15 +91,21 @@ def gather_context(cache: torch.Tensor, table_row: torch.Tensor, length: int) ->
 
 
 def attend(q_rows: torch.Tensor, q_pos: torch.Tensor, keys: torch.Tensor,
-           values: torch.Tensor, scale: float, causal: bool) -> torch.Tensor:
+           values: torch.Tensor, scale: float, causal: bool, window: int = 0,
+           softcap: float = 0.0, sinks: torch.Tensor | None = None) -> torch.Tensor:
     """Masked softmax attention of some query rows over one sequence's keys.
 
     q_rows: [T, Hq, D]; q_pos: [T] positions of those queries; keys, values:
     [L, Hkv, D] (positions 0..L-1). Query head h reads KV head h // (Hq/Hkv).
-    Key p is visible to a query at position t when p < L and, if causal, p <= t.
-    out[t, h] = sum_p w_p v_p / sum_p w_p with w_p = exp(s_p - max s) over the
-    visible p, s_p = scale * q.k_p; no visible key gives zeros.
-    Returns [T, Hq, D] float64.
+    Key p is visible to a query at position t when p < L, if causal p <= t, and
+    with a sliding window w > 0 also p > t - w ("32. Production attention
+    kernels", One kernel for the whole batch: the window's extra mask term).
+    Score s_p = scale * q.k_p, then, with a softcap c > 0, c * tanh(s_p / c)
+    ("poot - Attention and KV Cache", The streaming schedule: softcap_or_identity).
+    out[t, h] = sum_p e^{s_p} v_p / (e^{z_h} + sum_p e^{s_p}) over the visible p,
+    where the optional sink logit z_h joins the denominator only ("32. Production
+    attention kernels", Stretch exercises, attention sinks); without a sink the
+    e^{z_h} term is absent. No visible key gives zeros. Returns [T, Hq, D] float64.
     """
     T, Hq, D = q_rows.shape
     L, Hkv, _ = keys.shape
@@ -111,20 +117,30 @@ def attend(q_rows: torch.Tensor, q_pos: torch.Tensor, keys: torch.Tensor,
     if L == 0 or T == 0:
         return out
     key_pos = torch.arange(L, dtype=torch.long)
+    pos = q_pos.to(torch.long)[:, None]
     if causal:
-        visible = key_pos[None, :] <= q_pos.to(torch.long)[:, None]        # [T, L]
+        visible = key_pos[None, :] <= pos                                     # [T, L]
     else:
         visible = torch.ones((T, L), dtype=torch.bool)
+    if window > 0:
+        visible = visible & (key_pos[None, :] > pos - window)
     any_visible = visible.any(dim=1)                                         # [T]
     neg_inf = torch.tensor(-math.inf, dtype=_F64)
     for h in range(Hq):
         kv = h // group
         scores = scale * (q64[:, h, :] @ keys[:, kv, :].T)                  # [T, L]
+        if softcap > 0:
+            scores = softcap * torch.tanh(scores / softcap)
         scores = torch.where(visible, scores, neg_inf)
         row_max = scores.max(dim=1, keepdim=True).values
         row_max = torch.where(any_visible[:, None], row_max, torch.zeros_like(row_max))
+        if sinks is not None:
+            z = float(sinks[h])
+            row_max = torch.where(any_visible[:, None], torch.clamp(row_max, min=z), torch.full_like(row_max, z))
         weights = torch.where(visible, torch.exp(scores - row_max), torch.zeros_like(scores))
         denom = weights.sum(dim=1, keepdim=True)
+        if sinks is not None:
+            denom = denom + torch.exp(float(sinks[h]) - row_max)
         num = weights @ values[:, kv, :]                                     # [T, D]
         out[:, h, :] = torch.where(any_visible[:, None], num / torch.where(denom > 0, denom, 1.0),
                                    torch.zeros_like(num))
@@ -134,7 +150,8 @@ def attend(q_rows: torch.Tensor, q_pos: torch.Tensor, keys: torch.Tensor,
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            block_tables: torch.Tensor, context_lens: torch.Tensor,
                            scale: float | None = None,
-                           seqs: list[int] | None = None) -> torch.Tensor:
+                           seqs: list[int] | None = None, window: int = 0, softcap: float = 0.0,
+                           sinks: torch.Tensor | None = None) -> torch.Tensor:
     """One query per sequence over its first ``context_lens[s]`` cached positions.
 
     q: [S, Hq, D]; caches [num_blocks, block_size, Hkv, D]; block_tables
@@ -154,7 +171,8 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         keys = gather_context(k_cache, block_tables[s], length)
         values = gather_context(v_cache, block_tables[s], length)
         pos = torch.tensor([max(length - 1, 0)], dtype=torch.long)
-        out[s] = attend(q[s:s + 1], pos, keys, values, sc, causal=False)[0]
+        out[s] = attend(q[s:s + 1], pos, keys, values, sc, causal=False, window=window,
+                        softcap=softcap, sinks=sinks)[0]
     return out
 
 
@@ -162,7 +180,8 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
                            block_tables: torch.Tensor, causal: bool = True,
                            scale: float | None = None,
-                           tokens: torch.Tensor | None = None) -> torch.Tensor:
+                           tokens: torch.Tensor | None = None, window: int = 0,
+                           softcap: float = 0.0, sinks: torch.Tensor | None = None) -> torch.Tensor:
     """A flattened batch: request r owns query rows query_start_loc[r]..[r+1]-1.
 
     Its q_len queries are the newest q_len of its seq_lens[r] positions: query
@@ -190,5 +209,6 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         values = gather_context(v_cache, block_tables[r], length)
         idx = torch.tensor(rows, dtype=torch.long)
         pos = length - q_len + (idx - start)
-        out[idx] = attend(q.index_select(0, idx), pos, keys, values, sc, causal)
+        out[idx] = attend(q.index_select(0, idx), pos, keys, values, sc, causal, window=window,
+                          softcap=softcap, sinks=sinks)
     return out
