@@ -72,6 +72,24 @@ typedef enum pa_dtype {
 #define PA_ERRBIT_QUERY_LAYOUT       8  /* query_start_loc not monotone or q_len > seq_len: rows zeroed     */
 #define PA_ERRBIT_WAIT_TIMEOUT      16  /* an internal bounded wait expired: that tile's output is invalid */
 
+/* Optional score modifiers for the *_ex entry points (a NULL options pointer, or a
+ * zero-initialised struct, means none of them).
+ *   sliding_window > 0: a query at position t sees only keys at positions > t - sliding_window
+ *     (and <= t when causal). "32. Production attention kernels", One kernel for the whole
+ *     batch: the window's loop start and extra mask term.
+ *   logit_softcap > 0: every score s = scale * q.k becomes logit_softcap * tanh(s / logit_softcap)
+ *     before the softmax. "poot - Attention and KV Cache", The streaming schedule
+ *     (softcap_or_identity) and Implementation details.
+ *   sinks: NULL or a device pointer to Hq float32 sink logits (natural-log units): query head h's
+ *     softmax denominator gains e^{sinks[h]} and no value is added, so
+ *     out = sum_p e^{s_p} v_p / (e^{sinks[h]} + sum_p e^{s_p}). "32. Production attention
+ *     kernels", Stretch exercises, item 4 (attention sinks). Must be 4-byte aligned. */
+typedef struct pa_attn_options {
+  int32_t sliding_window;
+  float logit_softcap;
+  const float* sinks;
+} pa_attn_options;
+
 /* Human-readable name of a status code. Never NULL. */
 const char* pa_status_string(int status);
 
@@ -194,6 +212,28 @@ pa_status pa_paged_attention_decode_static_scratch(const void* q, const void* k_
                                                    int max_blocks_per_seq, float scale, pa_dtype dtype,
                                                    int num_splits, void* out, int32_t* error_word,
                                                    void* stream);
+
+/* pa_paged_attention_decode with score modifiers (see pa_attn_options; NULL = none). All other
+ * arguments, layouts and rules are those of pa_paged_attention_decode. */
+pa_status pa_paged_attention_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int num_blocks, int max_blocks_per_seq,
+                                       float scale, pa_dtype dtype, int num_splits,
+                                       void* out, void* workspace, size_t workspace_bytes,
+                                       const pa_attn_options* options, int32_t* error_word, void* stream);
+
+/* pa_paged_attention_varlen with score modifiers (see pa_attn_options; NULL = none). All other
+ * arguments, layouts and rules are those of pa_paged_attention_varlen. */
+pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* query_start_loc, const int32_t* seq_lens,
+                                       const int32_t* block_tables,
+                                       int num_reqs, int num_tokens, int max_query_len,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int num_blocks, int max_blocks_per_seq,
+                                       int causal, float scale, pa_dtype dtype,
+                                       void* out, const pa_attn_options* options, int32_t* error_word,
+                                       void* stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -9,6 +9,7 @@ them without the built library raises.
 
 from __future__ import annotations
 
+import ctypes
 import math
 
 import torch
@@ -88,6 +89,15 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_b
                                                      block_size, num_splits))
 
 
+def _options(window: int, softcap: float, sinks: torch.Tensor | None):
+    """pa_attn_options for the *_ex calls, or None when no modifier is asked for."""
+    if not window and not softcap and sinks is None:
+        return None
+    if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_cuda):
+        raise ValueError("sinks must be a float32 CUDA tensor of num_q_heads logits")
+    return ctypes.byref(_lib.AttnOptions(int(window), float(softcap), _ptr(sinks)))
+
+
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       slot_mapping: torch.Tensor, error_word: torch.Tensor | None = None,
                       stream: torch.cuda.Stream | None = None) -> None:
@@ -105,11 +115,13 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            scale: float | None = None, num_splits: int = 0,
                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                            error_word: torch.Tensor | None = None,
-                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+                           stream: torch.cuda.Stream | None = None, window: int = 0, softcap: float = 0.0,
+                           sinks: torch.Tensor | None = None) -> torch.Tensor:
     """One query per sequence over its paged context (split-KV + combine in the library).
 
     ``workspace`` (a byte or fp32 CUDA tensor) is allocated here when not given; pass one
-    to keep the call allocation-free (e.g. under CUDA-graph capture)."""
+    to keep the call allocation-free (e.g. under CUDA-graph capture). ``window``,
+    ``softcap`` and ``sinks`` are the pa_attn_options score modifiers."""
     s, hq, d = q.shape
     nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     mb = block_tables.shape[1]
@@ -119,10 +131,10 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.load().pa_paged_attention_decode(
+    st = _lib.load().pa_paged_attention_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         s, hq, hkv, d, bs, nb, mb, float(scale or 0.0), _dtype(q), int(num_splits),
-        _ptr(out), _ptr(workspace), ws_len, _ptr(error_word), _stream(stream))
+        _ptr(out), _ptr(workspace), ws_len, _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
     _check("pa_paged_attention_decode", st)
     return out
 
@@ -132,19 +144,21 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            block_tables: torch.Tensor, max_query_len: int, causal: bool = True,
                            scale: float | None = None, out: torch.Tensor | None = None,
                            error_word: torch.Tensor | None = None,
-                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+                           stream: torch.cuda.Stream | None = None, window: int = 0, softcap: float = 0.0,
+                           sinks: torch.Tensor | None = None) -> torch.Tensor:
     """Flattened prefill / verify / decode batch; request r's queries are the newest q_len of
-    its seq_lens[r] positions, causal by position."""
+    its seq_lens[r] positions, causal by position. ``window``, ``softcap`` and ``sinks`` are
+    the pa_attn_options score modifiers."""
     n, hq, d = q.shape
     nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     r = seq_lens.shape[0]
     mb = block_tables.shape[1]
     if out is None:
         out = torch.empty_like(q)
-    st = _lib.load().pa_paged_attention_varlen(
+    st = _lib.load().pa_paged_attention_varlen_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
         r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
-        _dtype(q), _ptr(out), _ptr(error_word), _stream(stream))
+        _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
     _check("pa_paged_attention_varlen", st)
     return out
 

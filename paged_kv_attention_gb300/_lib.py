@@ -25,6 +25,14 @@ PA_ERRBIT_WAIT_TIMEOUT = 16
 
 _i, _f, _p, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
+
+class AttnOptions(ctypes.Structure):
+    """pa_attn_options: sliding window, logit softcap, device pointer to per-head sink logits."""
+    _fields_ = [("sliding_window", ctypes.c_int32), ("logit_softcap", ctypes.c_float), ("sinks", ctypes.c_void_p)]
+
+
+_opt = ctypes.POINTER(AttnOptions)
+
 # name -> (restype, argtypes); mirrors include/paged_attn.h
 SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i]),
@@ -40,6 +48,10 @@ SIGNATURES = {
                                        _i, _f, _i, _p, _p, _p]),
     "pa_paged_attention_decode_static_scratch": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f,
                                                       _i, _i, _p, _p, _p]),
+    "pa_paged_attention_decode_ex": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                                          _p, _p, _sz, _opt, _p, _p]),
+    "pa_paged_attention_varlen_ex": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                          _i, _f, _i, _p, _opt, _p, _p]),
 }
 
 _lib = None

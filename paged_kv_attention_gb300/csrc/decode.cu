@@ -28,7 +28,8 @@ namespace {
 
 // ------------------------------------------------------------------ unit resolution
 struct Unit {
-  int len;        // keys visible to every row of the unit: positions [0, len)
+  int len;        // keys visible to every row of the unit: positions [start, len)
+  int start;      // first visible position (> 0 only under a sliding window)
   int table_row;  // block table row
   int q_row;      // row of q / out
 };
@@ -40,6 +41,7 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     u.table_row = unit;
     u.q_row = unit;
     len = p.context_lens[unit];
+    u.start = 0;
   } else {
     // request r with query_start_loc[r] <= unit < query_start_loc[r+1]
     int lo = 0, hi = p.num_reqs;
@@ -53,6 +55,7 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     const int q_len = stop - start;
     u.table_row = lo;
     u.q_row = unit;
+    u.start = 0;
     if (unit < start || unit >= stop || q_len > seq) {
       if (report) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
       len = 0;
@@ -62,6 +65,7 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     } else {
       const int pos = seq - q_len + (unit - start);  // queries are the newest positions
       len = p.causal ? pos + 1 : seq;
+      if (p.window > 0) u.start = max(0, pos - p.window + 1);
     }
   }
   const int cap = p.max_blocks * p.block_size;
@@ -70,7 +74,16 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     len = len < 0 ? 0 : cap;
   }
   u.len = len;
+  // decode: the query is the newest cached position, len - 1
+  if (!p.varlen && p.window > 0) u.start = max(0, len - p.window);
+  if (u.start > u.len) u.start = u.len;
   return u;
+}
+
+// Score in log2 units: s * scale * log2 e, or with a softcap c: c * tanh(s * scale / c) * log2 e
+// ("poot - Attention and KV Cache", The streaming schedule: softcap_or_identity).
+__device__ __forceinline__ float score_log2(const DecodeParams& p, float s) {
+  return p.softcap_log2 > 0.f ? p.softcap_log2 * tanhf(s * p.scale_over_cap) : s * p.scale_log2;
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -95,6 +108,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, const flo
       O += wt * mo[(w * rows + n) * D + d];
     }
     if (p.num_splits == 1) {
+      if (p.sinks != nullptr) O *= fold_sink(p.sinks[h0 + n], M, L);
       const float v = (L > 0.f) ? O / L : 0.f;
       OutT* out = reinterpret_cast<OutT*>(p.out);
       out[((size_t)q_row * p.num_q_heads + h0 + n) * D + d] = static_cast<OutT>(v);
@@ -173,8 +187,8 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
 
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
   const int n_chunks = (u.len + kChunk - 1) / kChunk;
-  const int c_begin = split * p.chunks_per_split;
-  const int c_end = min(n_chunks, c_begin + p.chunks_per_split);
+  const int c_begin = max(split * p.chunks_per_split, u.start / kChunk);
+  const int c_end = min(n_chunks, split * p.chunks_per_split + p.chunks_per_split);
   const int n_mine = max(0, c_end - c_begin);
 
   if (threadIdx.x == 0) {
@@ -266,6 +280,7 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
       uint8_t* vt = kt + C::kTileBytes;
       const int key0 = (c_begin + i) * kChunk;
       const int nvalid = min(kChunk, u.len - key0);
+      const int nlow = u.start - key0;  // keys below this index of the chunk are outside the window
       if (nvalid < kChunk) {
         // rows past the sequence end may hold anything (NaN included): zero them so that
         // 0-probability keys contribute exactly 0 to P.V (a select, not a multiply)
@@ -295,9 +310,17 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float x0 = s[nt][0] * sl2, x1 = s[nt][1] * sl2, x2 = s[nt][2] * sl2, x3 = s[nt][3] * sl2;
-        if (g4 >= nvalid) x0 = x1 = -INFINITY;
-        if (g4 + 8 >= nvalid) x2 = x3 = -INFINITY;
+        float x0, x1, x2, x3;
+        if (p.softcap_log2 > 0.f) {
+          x0 = score_log2(p, s[nt][0]);
+          x1 = score_log2(p, s[nt][1]);
+          x2 = score_log2(p, s[nt][2]);
+          x3 = score_log2(p, s[nt][3]);
+        } else {
+          x0 = s[nt][0] * sl2, x1 = s[nt][1] * sl2, x2 = s[nt][2] * sl2, x3 = s[nt][3] * sl2;
+        }
+        if (g4 >= nvalid || g4 < nlow) x0 = x1 = -INFINITY;
+        if (g4 + 8 >= nvalid || g4 + 8 < nlow) x2 = x3 = -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -401,8 +424,8 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
-  const int k_begin = split * p.chunks_per_split * kChunk;
-  const int k_end = min(u.len, k_begin + p.chunks_per_split * kChunk);
+  const int k_begin = max(split * p.chunks_per_split * kChunk, u.start);
+  const int k_end = min(u.len, split * p.chunks_per_split * kChunk + p.chunks_per_split * kChunk);
 
   const float* qg = reinterpret_cast<const float*>(p.q) + ((size_t)u.q_row * p.num_q_heads + (size_t)kvh * G) * D;
   for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) q_s[idx] = (idx / D < G) ? qg[idx] : 0.f;
@@ -452,7 +475,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
     my_vrow[lane] = valid ? row : -2;
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
-      const float x = valid ? s[g] * p.scale_log2 : -INFINITY;
+      const float x = valid ? score_log2(p, s[g]) : -INFINITY;
       float mx = x;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -519,27 +542,39 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   float M = m_s;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // a sink logit joins the denominator here, once, not in every split
+  const float z2 = p.sinks != nullptr ? p.sinks[h] * kLog2e : -INFINITY;
+  M = fmaxf(M, z2);
   const float Mu = (M == -INFINITY) ? 0.f : M;
   const float w = (lane < S) ? exp2f(m_s - Mu) : 0.f;
   float L = w * l_s;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  L += exp2f(z2 - Mu);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)unit * p.num_q_heads + h) * D;
-  for (int d = lane * 4; d < D; d += 128) {
+  // every lane runs every iteration (the weight shuffles need the whole warp); lanes past
+  // the head dim only skip their loads and stores
+  for (int d0 = 0; d0 < D; d0 += 128) {
+    const int d = d0 + lane * 4;
+    const bool active = d < D;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < S; ++s) {
       const float ws = __shfl_sync(0xffffffffu, w, s);
-      const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)s * p.num_q_heads) * D + d);
-      a.x = fmaf(ws, v.x, a.x);
-      a.y = fmaf(ws, v.y, a.y);
-      a.z = fmaf(ws, v.z, a.z);
-      a.w = fmaf(ws, v.w, a.w);
+      if (active) {
+        const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)s * p.num_q_heads) * D + d);
+        a.x = fmaf(ws, v.x, a.x);
+        a.y = fmaf(ws, v.y, a.y);
+        a.z = fmaf(ws, v.z, a.z);
+        a.w = fmaf(ws, v.w, a.w);
+      }
     }
-    out[d] = static_cast<OutT>(a.x * inv);
-    out[d + 1] = static_cast<OutT>(a.y * inv);
-    out[d + 2] = static_cast<OutT>(a.z * inv);
-    out[d + 3] = static_cast<OutT>(a.w * inv);
+    if (active) {
+      out[d] = static_cast<OutT>(a.x * inv);
+      out[d + 1] = static_cast<OutT>(a.y * inv);
+      out[d + 2] = static_cast<OutT>(a.z * inv);
+      out[d + 3] = static_cast<OutT>(a.w * inv);
+    }
   }
 }
 

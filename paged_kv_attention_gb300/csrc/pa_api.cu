@@ -273,12 +273,50 @@ extern "C" int pa_decode_auto_splits(int num_seqs, int num_q_heads, int num_kv_h
   return auto_splits(info, num_seqs, num_kv_heads, head_dim, num_q_heads / num_kv_heads, max_chunks, dtype);
 }
 
+namespace {
+
+// Checks and applies pa_attn_options (NULL = none) to the score-modifier fields of p.
+template <typename Params>
+pa_status apply_options(const pa_attn_options* o, float scale, Params& p) {
+  p.window = 0;
+  p.softcap_log2 = 0.f;
+  p.scale_over_cap = 0.f;
+  p.sinks = nullptr;
+  if (o == nullptr) return PA_OK;
+  if (o->sliding_window < 0) return PA_ERR_INVALID_ARGUMENT;
+  if (!(o->logit_softcap >= 0.f) || isinf(o->logit_softcap)) return PA_ERR_INVALID_ARGUMENT;
+  if (o->sinks != nullptr && (reinterpret_cast<uintptr_t>(o->sinks) & 3u) != 0) return PA_ERR_INVALID_ARGUMENT;
+  p.window = o->sliding_window;
+  if (o->logit_softcap > 0.f) {
+    p.softcap_log2 = o->logit_softcap * kLog2e;
+    p.scale_over_cap = scale / o->logit_softcap;
+  }
+  p.sinks = o->sinks;
+  return PA_OK;
+}
+
+}  // namespace
+
 extern "C" pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
                                                const int32_t* block_tables, const int32_t* context_lens,
                                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                                int block_size, int num_blocks, int max_blocks_per_seq, float scale,
                                                pa_dtype dtype, int num_splits, void* out, void* workspace,
                                                size_t workspace_bytes, int32_t* error_word, void* stream) {
+  return pa_paged_attention_decode_ex(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
+                                      dtype, num_splits, out, workspace, workspace_bytes, nullptr, error_word,
+                                      stream);
+}
+
+extern "C" pa_status pa_paged_attention_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                                                  const int32_t* block_tables, const int32_t* context_lens,
+                                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, int num_blocks, int max_blocks_per_seq,
+                                                  float scale, pa_dtype dtype, int num_splits, void* out,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  const pa_attn_options* options, int32_t* error_word,
+                                                  void* stream) {
   if (num_seqs < 0 || num_splits < 0 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0) return PA_OK;
   if (!context_lens) return PA_ERR_INVALID_ARGUMENT;
@@ -306,6 +344,8 @@ extern "C" pa_status pa_paged_attention_decode(const void* q, const void* k_cach
   p.max_blocks = max_blocks_per_seq;
   const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
   p.scale_log2 = sc * kLog2e;
+  st = apply_options(options, sc, p);
+  if (st != PA_OK) return st;
   return run_decode_units(p, dtype, k_cache, v_cache, num_splits, workspace, workspace_bytes, as_stream(stream));
 }
 
@@ -316,6 +356,20 @@ extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cach
                                                int block_size, int num_blocks, int max_blocks_per_seq, int causal,
                                                float scale, pa_dtype dtype, void* out, int32_t* error_word,
                                                void* stream) {
+  return pa_paged_attention_varlen_ex(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, num_reqs,
+                                      num_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      num_blocks, max_blocks_per_seq, causal, scale, dtype, out, nullptr,
+                                      error_word, stream);
+}
+
+extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
+                                                  const int32_t* query_start_loc, const int32_t* seq_lens,
+                                                  const int32_t* block_tables, int num_reqs, int num_tokens,
+                                                  int max_query_len, int num_q_heads, int num_kv_heads,
+                                                  int head_dim, int block_size, int num_blocks,
+                                                  int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
+                                                  void* out, const pa_attn_options* options, int32_t* error_word,
+                                                  void* stream) {
   if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_reqs == 0 || num_tokens == 0) return PA_OK;
   if (!query_start_loc || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
@@ -347,6 +401,8 @@ extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cach
     vp.q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
     vp.causal = causal ? 1 : 0;
     vp.scale_log2 = sc * kLog2e;
+    st = apply_options(options, sc, vp);
+    if (st != PA_OK) return st;
     CUtensorMap qmap, kmap, vmap;
     if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile) ||
         !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks,
@@ -379,5 +435,7 @@ extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cach
   p.num_blocks = num_blocks;
   p.max_blocks = max_blocks_per_seq;
   p.scale_log2 = sc * kLog2e;
+  st = apply_options(options, sc, p);
+  if (st != PA_OK) return st;
   return run_decode_units(p, dtype, k_cache, v_cache, 1, nullptr, 0, s);
 }

@@ -104,6 +104,19 @@ __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Fold a per-head sink logit z (natural-log units; it joins the softmax denominator and
+// contributes no value) into a merged state (M in log2 units, L, and the accumulators the
+// caller scales by the returned factor): M' = max(M, z log2 e), L' = L 2^(M - M') + 2^(z log2 e - M').
+__device__ __forceinline__ float fold_sink(float z, float& M, float& L) {
+  const float z2 = z * kLog2e;
+  const float Mn = fmaxf(M, z2);
+  if (Mn == -INFINITY) return 1.f;  // no keys and no (finite) sink: nothing changes
+  const float f = exp2f(M - Mn);
+  L = L * f + exp2f(z2 - Mn);
+  M = Mn;
+  return f;
+}
+
 // Offset of the 16-byte unit `unit` (0..7) of row `row` inside a 128-byte-swizzled tile
 // whose rows are 128 bytes: the unit index is XORed with the row's position in its
 // 8-row (1024-byte) group, the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B.

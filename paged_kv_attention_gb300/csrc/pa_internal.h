@@ -42,6 +42,11 @@ struct DecodeParams {
   int num_splits;
   int chunks_per_split;
   float scale_log2;  // softmax scale * log2(e)
+  // score modifiers (pa_attn_options)
+  int window;            // > 0: a query at position t sees keys at positions > t - window
+  float softcap_log2;    // > 0: score -> softcap * tanh(scale * s / softcap), in log2 units (* log2 e)
+  float scale_over_cap;  // scale / softcap
+  const float* sinks;    // nullable [Hq]: per-head sink logit (natural-log units)
 };
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
@@ -79,6 +84,10 @@ struct VarlenParams {
   int q_tiles;  // cdiv(max_query_len, tokens per CTA)
   int causal;
   float scale_log2;
+  int window;
+  float softcap_log2;
+  float scale_over_cap;
+  const float* sinks;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
 int varlen_tc_tokens_per_cta(int group);

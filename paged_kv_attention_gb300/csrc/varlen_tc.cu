@@ -174,6 +174,14 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
+// tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1): one ex2 and one approximate reciprocal; absolute
+// error ~1e-7 (the softcap multiplies it by the cap), exact limits +-1 at +-infinity.
+__device__ __forceinline__ float tanh_ex2(float y) {
+  const float e = ex2(y * 2.8853900817779268f);
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.f));
+  return 1.f - 2.f * r;
+}
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -255,7 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const TileSpan spanA = tile_span(tok0, TOK, q_len, seq_len, p.causal);
   const TileSpan spanB = tile_span(tok0 + TOK, TOK, q_len, seq_len, p.causal);
-  const int n_kv = max(spanA.n_kv, spanB.n_kv);
+  // Iteration i covers key tile j0 + i. Under a sliding window, j0 is the tile holding the
+  // oldest key the CTA's first query sees; tiles before it are never loaded.
+  const int j0 = p.window > 0 ? max(0, spanA.first - p.window + 1) / kBN : 0;
+  const int nA = spanA.n_kv - j0;
+  const int nB = spanB.n_kv > 0 ? spanB.n_kv - j0 : 0;
+  const int n_kv = max(nA, nB);
   const int bs = p.block_size;
   const int pages_per_tile = kBN / bs;
   const int seq_pages = (seq_len + bs - 1) / bs;
@@ -302,13 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
                       q_start + tok0 + t * TOK);
       const int32_t* table = p.block_tables + (size_t)r * p.max_blocks;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % kStages;
-        const uint32_t round_parity = ((j / kStages) - 1) & 1;
-        const int p0 = j * pages_per_tile;
+      for (int i = 0; i < n_kv; ++i) {
+        const int st = i % kStages;
+        const uint32_t round_parity = ((i / kStages) - 1) & 1;
+        const int p0 = (j0 + i) * pages_per_tile;
         const int p1 = min(p0 + pages_per_tile, seq_pages);
         const uint32_t bytes = (uint32_t)(p1 - p0) * bs * 256u;
-        if (j >= kStages && !wait_or_abort(&bars[B_KE + st], round_parity, abort_flag)) {
+        if (i >= kStages && !wait_or_abort(&bars[B_KE + st], round_parity, abort_flag)) {
           set_abort(abort_flag, p.err);
           break;
         }
@@ -320,9 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + (pg - p0) * bs * 128, &kmap,
                         &bars[B_KF + st], a * 64, kvh, 0, page);
         }
-        if (j >= kStages && !wait_or_abort(&bars[B_VE + st], round_parity, abort_flag)) {
+        if (i >= kStages && !wait_or_abort(&bars[B_VE + st], round_parity, abort_flag)) {
           set_abort(abort_flag, p.err);
-          *issued_tiles = j + 1;  // K of tile j is in flight
+          *issued_tiles = i + 1;  // K of iteration i is in flight
           break;
         }
         mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
@@ -332,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + (pg - p0) * bs * 128, &vmap,
                         &bars[B_VF + st], a * 64, kvh, 0, page);
         }
-        *issued_tiles = j + 1;
+        *issued_tiles = i + 1;
       }
     }
   } else if (warp == 9) {
@@ -342,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = smem_addr(smem + kOffQ);
     const uint32_t sK = smem_addr(smem + kOffK);
     const uint32_t sV = smem_addr(smem + kOffV);
-    const int nA = spanA.n_kv, nB = spanB.n_kv;
     // Descriptors advance by adding (byte offset >> 4) to the start-address field; every
     // operand lies below 256 KiB of the shared window, so the 14-bit field never carries.
     const uint64_t dq0 = sdesc(sQ, 16, 1024);
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; ok && j < n_kv; ++j) {
       const int st = j % kStages;
       if (!(ok = warp_wait(&bars[B_VF + st], (j / kStages) & 1, abort_flag))) break;
-      const int zero_from = seq_len - j * kBN;  // V rows at or past the sequence end: exact zeros
+      const int zero_from = seq_len - (j0 + j) * kBN;  // V rows at or past the sequence end: exact zeros
       if (zero_from < kBN) {
         uint8_t* vbp = smem + kOffV + st * kTileBytes;
         const int rows = kBN - zero_from;
@@ -428,26 +440,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ softmax: warps 0-3 tile A, 4-7 tile B
     const int t = warp >> 2;
-    const TileSpan span = t == 0 ? spanA : spanB;
+    const int n_mine = t == 0 ? nA : nB;
     const int row = tid & (kBM - 1);
     const int tok = tok0 + t * TOK + row / G;
     const bool row_valid = tok < q_len;
     const int qpos = seq_len - q_len + tok;
     const int vis_end = p.causal ? min(qpos + 1, seq_len) : seq_len;
+    const int vis_start = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
+    const bool capped = p.softcap_log2 > 0.f;
     const float c = p.scale_log2;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + col_s(t);
     const uint32_t o_col = lane_base + col_o(t);
-    float m_run = -INFINITY, l_run = 0.f;
+    // a sink logit starts the running state: it joins the denominator and adds no value
+    float m_run = p.sinks != nullptr ? p.sinks[kvh * G + row % G] * kLog2e : -INFINITY;
+    float l_run = p.sinks != nullptr ? 1.f : 0.f;
     bool ok = true;
-    for (int j = 0; j < span.n_kv; ++j) {
+    for (int j = 0; j < n_mine; ++j) {
       if (!warp_wait(&bars[B_SF + t], j & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int nvis = vis_end - j * kBN;  // keys of this tile the row may see
-      const bool full = nvis >= kBN;
+      const int nvis = vis_end - (j0 + j) * kBN;  // keys below this index of the tile are not too new
+      const int nlo = vis_start - (j0 + j) * kBN;  // keys from this index on are inside the window
+      const bool full = nvis >= kBN && nlo <= 0;
       // the row's 128 scores, one TMEM round trip (tcgen05.wait::ld waits for every load)
       uint32_t sv[4][32];
 #pragma unroll
@@ -458,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
           for (int i = 0; i < 32; ++i)  // select: NaN past the sequence end never survives
-            sv[q4][i] = (q4 * 32 + i < nvis) ? sv[q4][i] : __float_as_uint(-INFINITY);
+            sv[q4][i] = (q4 * 32 + i < nvis && q4 * 32 + i >= nlo) ? sv[q4][i] : __float_as_uint(-INFINITY);
       }
       // row maximum over eight interleaved chains (short dependency chains)
       float mx8[8];
@@ -470,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[q4][i]));
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float mxs = mx * c;
+      // the softcap is increasing, so the capped maximum is the cap of the maximum
+      const float mxs = capped ? (mx == -INFINITY ? -INFINITY : p.softcap_log2 * tanh_ex2(mx * p.scale_over_cap))
+                               : mx * c;
       float m_new = m_run, alpha = 1.f;
       bool rescale = false;
       if (m_run == -INFINITY || mxs > m_run + kRescaleThreshold) {
@@ -491,7 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t* src = sv[2 * h + (i >> 4)];
           const int e = (2 * i) & 31;
           float x0, x1;
-          f2_split(f2_fma(f2(__uint_as_float(src[e]), __uint_as_float(src[e + 1])), c2, nmu2), x0, x1);
+          if (capped) {  // masked keys hold -inf: tanh gives -1, the select below zeroes them
+            x0 = p.softcap_log2 * tanh_ex2(__uint_as_float(src[e]) * p.scale_over_cap) - mu;
+            x1 = p.softcap_log2 * tanh_ex2(__uint_as_float(src[e + 1]) * p.scale_over_cap) - mu;
+            x0 = __uint_as_float(src[e]) == -INFINITY ? -INFINITY : x0;
+            x1 = __uint_as_float(src[e + 1]) == -INFINITY ? -INFINITY : x1;
+          } else {
+            f2_split(f2_fma(f2(__uint_as_float(src[e]), __uint_as_float(src[e + 1])), c2, nmu2), x0, x1);
+          }
           const float p0 = ex2(x0), p1 = ex2(x1);  // 2^-inf = 0 for masked keys
           sum2[i & 1] = f2_add(sum2[i & 1], f2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);  // key 64h + 2i in the low half, 64h + 2i + 1 in the high half
@@ -520,10 +546,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars[B_PR + t]);
     }
-    if (ok && span.n_kv > 0 && !warp_wait(&bars[B_OD + t], (span.n_kv - 1) & 1, abort_flag)) ok = false;
+    if (ok && n_mine > 0 && !warp_wait(&bars[B_OD + t], (n_mine - 1) & 1, abort_flag)) ok = false;
     if (!ok) {
       set_abort(abort_flag, p.err);
-    } else if (span.n_kv > 0) {
+    } else if (n_mine > 0) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) +

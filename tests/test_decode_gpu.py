@@ -41,6 +41,20 @@ def test_split_counts(dtype, splits):
     check_close(out, oracle_decode(case, ko, vo), dtype, label=f"splits={splits}")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("splits", [17, 20, 32])
+def test_many_splits(dtype, head_dim, splits):
+    """More than 16 splits: the combine's per-split weights come from lanes 16-31 too."""
+    hq, hkv = (16, 4) if dtype == torch.bfloat16 or head_dim < 256 else (8, 4)
+    case = workloads.decode_case("many", 150 + head_dim + splits, [1, 333, 1500, 4096], num_q_heads=hq,
+                                 num_kv_heads=hkv, head_dim=head_dim, block_size=16, dtype=dtype)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    out = run_decode(case, kc, vc, splits)
+    check_close(out, oracle_decode(case, ko, vo), dtype, label=f"D{head_dim} splits={splits}")
+
+
 @pytest.mark.parametrize("head_dim", [64, 128, 256])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (12, 4), (16, 4), (32, 4), (32, 2)])
 @pytest.mark.parametrize("block_size", [16, 32, 64])
