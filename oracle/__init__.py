@@ -16,6 +16,7 @@ forms, invariants, a brute-force pool scan, a torch SDPA special case and a
 hand-written golden fixture); no function is "parity unpinned".
 """
 
+from . import quant  # noqa: F401
 from .attention import (  # noqa: F401
     attend,
     default_scale,
