@@ -61,7 +61,9 @@ typedef enum pa_status {
 
 typedef enum pa_dtype {
   PA_DTYPE_F32 = 0,
-  PA_DTYPE_BF16 = 1
+  PA_DTYPE_BF16 = 1,
+  PA_DTYPE_INT8 = 2,      /* 8-bit cache codes (the *_quant calls only) */
+  PA_DTYPE_FP8_E4M3 = 3   /* 8-bit cache codes (the *_quant calls only) */
 } pa_dtype;
 
 /* Bits a kernel ORs into *error_word (see conventions above). */
@@ -234,6 +236,51 @@ pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const
                                        int causal, float scale, pa_dtype dtype,
                                        void* out, const pa_attn_options* options, int32_t* error_word,
                                        void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * 8-bit KV cache. "32. Production attention kernels", Quantized KV caches; "TileInfer.jl -
+ * Attention kernels", INT8 cache. The pools hold one code per element ([num_blocks,
+ * block_size, Hkv, D], int8 or fp8 E4M3) and one float32 scale per (slot, KV head)
+ * ([num_blocks, block_size, Hkv]); value = code * scale.
+ * --------------------------------------------------------------------------------------- */
+
+/* Quantise and write: for token i with slot = slot_mapping[i] >= 0 and each KV head, computed
+ * in float32 exactly as the page does: amax = max(max_d |x|, 1e-8), scale = amax / q_max
+ * (q_max 127 for PA_DTYPE_INT8, 448 for PA_DTYPE_FP8_E4M3), code = round-half-even(x / scale)
+ * clamped to +-127 (int8) or x / scale rounded to nearest E4M3 (fp8); the codes go to
+ * k_cache/v_cache[slot / block_size, slot % block_size] and the scale to k_scales/v_scales at
+ * the same place. key, value: [num_tokens, Hkv, D] of src_dtype (bf16 or f32). Slot -1 writes
+ * nothing; a slot outside the pool is skipped and flagged. head_dim must be a multiple of 32. */
+pa_status pa_reshape_and_cache_quant(const void* key, const void* value, pa_dtype src_dtype,
+                                     void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                     pa_dtype cache_dtype, const int32_t* slot_mapping, int num_tokens,
+                                     int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     int32_t* error_word, void* stream);
+
+/* Decode over an 8-bit cache: as pa_paged_attention_decode_ex (q and out bf16), with keys and
+ * values dequantised in registers: codes are exact in bf16, a key's scale multiplies its
+ * scores and a value's scale its probabilities before P.V. Supported: D in {128, 256},
+ * Hq/Hkv <= 16, block_size % 16 == 0. */
+pa_status pa_paged_attention_decode_quant(const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scales, const float* v_scales, pa_dtype cache_dtype,
+                                          const int32_t* block_tables, const int32_t* context_lens,
+                                          int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, int max_blocks_per_seq,
+                                          float scale, int num_splits, void* out, void* workspace,
+                                          size_t workspace_bytes, const pa_attn_options* options,
+                                          int32_t* error_word, void* stream);
+
+/* Varlen over an 8-bit cache: as pa_paged_attention_varlen_ex (q and out bf16); every query
+ * token runs as a one-split decode over the keys it sees (correct at any size; the tensor-core
+ * varlen kernel reads bf16 caches only). Supported shapes as pa_paged_attention_decode_quant. */
+pa_status pa_paged_attention_varlen_quant(const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scales, const float* v_scales, pa_dtype cache_dtype,
+                                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                                          const int32_t* block_tables, int num_reqs, int num_tokens,
+                                          int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, int max_blocks_per_seq, int causal,
+                                          float scale, void* out, const pa_attn_options* options,
+                                          int32_t* error_word, void* stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

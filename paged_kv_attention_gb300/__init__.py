@@ -23,6 +23,9 @@ __all__ = [
     "plan_decode_splits",
     "paged_attention_decode",
     "paged_attention_varlen",
+    "paged_attention_decode_quant",
+    "paged_attention_varlen_quant",
+    "reshape_and_cache_quant",
     "reshape_and_cache",
     "status_string",
     "supports",
@@ -160,6 +163,79 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
         _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
     _check("pa_paged_attention_varlen", st)
+    return out
+
+
+# ----------------------------------------------------------------------------- 8-bit caches
+_CODES = {torch.int8: _lib.PA_DTYPE_INT8, torch.float8_e4m3fn: _lib.PA_DTYPE_FP8_E4M3}
+
+
+def _cache_kind(t: torch.Tensor) -> int:
+    try:
+        return _CODES[t.dtype]
+    except KeyError:
+        raise PagedAttentionError("cache dtype", _lib.PA_ERR_UNSUPPORTED) from None
+
+
+def reshape_and_cache_quant(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            k_scales: torch.Tensor, v_scales: torch.Tensor, slot_mapping: torch.Tensor,
+                            error_word: torch.Tensor | None = None,
+                            stream: torch.cuda.Stream | None = None) -> None:
+    """Quantise key/value rows (bf16 or fp32) into int8 / fp8 code pools plus per-(slot, head)
+    fp32 scales, through the slot mapping."""
+    n, hkv, d = key.shape
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
+    st = _lib.load().pa_reshape_and_cache_quant(
+        _ptr(key), _ptr(value), _dtype(key), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+        _cache_kind(k_cache), _ptr(slot_mapping), n, hkv, d, bs, nb, _ptr(error_word), _stream(stream))
+    _check("pa_reshape_and_cache_quant", st)
+
+
+def paged_attention_decode_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 k_scales: torch.Tensor, v_scales: torch.Tensor, block_tables: torch.Tensor,
+                                 context_lens: torch.Tensor, scale: float | None = None, num_splits: int = 0,
+                                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                 error_word: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None,
+                                 window: int = 0, softcap: float = 0.0,
+                                 sinks: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode over an int8 / fp8 cache (q, out bf16)."""
+    s, hq, d = q.shape
+    nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = decode_workspace_bytes(s, hq, d, mb, bs, num_splits)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().pa_paged_attention_decode_quant(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales), _cache_kind(k_cache),
+        _ptr(block_tables), _ptr(context_lens), s, hq, hkv, d, bs, nb, mb, float(scale or 0.0), int(num_splits),
+        _ptr(out), _ptr(workspace), ws_len, _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
+    _check("pa_paged_attention_decode_quant", st)
+    return out
+
+
+def paged_attention_varlen_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 k_scales: torch.Tensor, v_scales: torch.Tensor, query_start_loc: torch.Tensor,
+                                 seq_lens: torch.Tensor, block_tables: torch.Tensor, max_query_len: int,
+                                 causal: bool = True, scale: float | None = None, out: torch.Tensor | None = None,
+                                 error_word: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None,
+                                 window: int = 0, softcap: float = 0.0,
+                                 sinks: torch.Tensor | None = None) -> torch.Tensor:
+    """Varlen attention over an int8 / fp8 cache (q, out bf16)."""
+    n, hq, d = q.shape
+    nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    r = seq_lens.shape[0]
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    st = _lib.load().pa_paged_attention_varlen_quant(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales), _cache_kind(k_cache),
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables), r, n, int(max_query_len), hq, hkv, d, bs, nb, mb,
+        int(bool(causal)), float(scale or 0.0), _ptr(out), _options(window, softcap, sinks), _ptr(error_word),
+        _stream(stream))
+    _check("pa_paged_attention_varlen_quant", st)
     return out
 
 

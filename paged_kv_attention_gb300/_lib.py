@@ -16,6 +16,8 @@ PA_ERR_CUDA = 4
 
 PA_DTYPE_F32 = 0
 PA_DTYPE_BF16 = 1
+PA_DTYPE_INT8 = 2
+PA_DTYPE_FP8_E4M3 = 3
 
 PA_ERRBIT_PAGE_OUT_OF_POOL = 1
 PA_ERRBIT_LENGTH_OUT_OF_RANGE = 2
@@ -50,6 +52,11 @@ SIGNATURES = {
                                                       _i, _i, _p, _p, _p]),
     "pa_paged_attention_decode_ex": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
                                           _p, _p, _sz, _opt, _p, _p]),
+    "pa_reshape_and_cache_quant": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _p, _p]),
+    "pa_paged_attention_decode_quant": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f,
+                                             _i, _p, _p, _sz, _opt, _p, _p]),
+    "pa_paged_attention_varlen_quant": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
+                                             _i, _i, _i, _f, _p, _opt, _p, _p]),
     "pa_paged_attention_varlen_ex": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                           _i, _f, _i, _p, _opt, _p, _p]),
 }

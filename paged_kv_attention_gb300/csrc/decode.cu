@@ -20,6 +20,9 @@
 // from the limit; the point of the MMA is to keep the issue slots free for the memory
 // pipeline. The probabilities are moved from the score accumulator layout to the P.V
 // operand layout with movmatrix (an in-register 8x8 transpose), without shared memory.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -147,34 +150,91 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
-template <int D>
-struct Bf16Cfg {
+// QK selects the cache format: 0 = bf16 values; 1 = int8 codes, 2 = fp8 E4M3 codes, each with
+// one fp32 scale per (slot, KV head). 8-bit codes are converted to bf16 in shared memory (exact:
+// |code| <= 127, and every E4M3 value is a bf16 value); the key's scale multiplies its scores
+// and the value's scale its probabilities before P.V ("TileInfer.jl - Attention kernels",
+// INT8 cache).
+template <int D, int QK>
+struct DecCfg {
   static constexpr int kConsumers = 4;
   static constexpr int kThreads = (kConsumers + 1) * 32;
-  static constexpr int kDChunks = D / 64;                 // 128-byte swizzle columns
-  static constexpr int kTileBytes = kChunk * D * 2;       // K or V rows of one stage
+  static constexpr int kElt = QK ? 1 : 2;                // bytes per cached element
+  static constexpr int kBoxes = D * kElt / 128;          // 128-byte swizzle columns of a cached row
+  static constexpr int kDChunks = D / 64;                // 128-byte columns of a bf16 row
+  static constexpr int kTileBytes = kChunk * D * kElt;   // K or V rows of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = (D == 64) ? 16 : (D == 128 ? 8 : 4);  // 64 KiB ring
+  static constexpr int kStages = 65536 / kStageBytes;    // 64 KiB ring
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMT = D / 16;
-  // barriers + merge (m, l) after the ring; the merge accumulators alias the ring
-  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kConsumers * 16 * 2 * 4;
+  static constexpr int kStagingBytes = QK ? kConsumers * 2 * kChunk * D * 2 : 0;  // bf16 K and V per consumer
+  static constexpr int kScaleBytes = QK ? kStages * 32 * 4 : 0;                   // 16 K + 16 V scales per stage
+  // ring | staging | full, empty barriers | merge (m, l) | scales; the merge accumulators alias the ring
+  static constexpr int kSmemBytes =
+      1024 + kRingBytes + kStagingBytes + 2 * kStages * 8 + kConsumers * 16 * 2 * 4 + kScaleBytes;
+  static_assert(kBoxes >= 1, "a cached row must span at least one 128-byte column");
   static_assert(kStages % kConsumers == 0, "stages are dealt to consumers round robin");
   static_assert(kConsumers * 16 * D * 4 <= kRingBytes, "merge area must fit in the ring");
 };
 
-template <int D, int NT>
-__global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
-    decode_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap) {
-  using C = Bf16Cfg<D>;
+// 16 codes (one 16-byte unit) -> 16 bf16 (two 16-byte units), exactly.
+template <int QK>
+__device__ __forceinline__ void codes_to_bf16(uint4 raw, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (QK == 1) {
+      const float f0 = (float)(int8_t)(w[k] & 0xffu), f1 = (float)(int8_t)((w[k] >> 8) & 0xffu);
+      const float f2 = (float)(int8_t)((w[k] >> 16) & 0xffu), f3 = (float)(int8_t)(w[k] >> 24);
+      o[2 * k] = pack_bf16x2(f0, f1);
+      o[2 * k + 1] = pack_bf16x2(f2, f3);
+    } else {
+      const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] & 0xffffu), __NV_E4M3);
+      const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] >> 16), __NV_E4M3);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+      o[2 * k] = pack_bf16x2(a.x, a.y);
+      o[2 * k + 1] = pack_bf16x2(b.x, b.y);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// A 16-row tile of codes (kBoxes swizzled 128-byte columns) -> the bf16 tile layout the MMA
+// path reads (kDChunks swizzled 128-byte columns). Rows at or past `valid_rows` become zeros.
+template <int D, int QK>
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int valid_rows, int lane) {
+  using C = DecCfg<D, QK>;
+  for (int idx = lane; idx < kChunk * C::kBoxes * 8; idx += 32) {
+    const int row = idx / (C::kBoxes * 8);
+    const int rest = idx - row * (C::kBoxes * 8);
+    const int box = rest >> 3, unit = rest & 7;  // codes 128 * box + 16 * unit .. + 15
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (row < valid_rows) codes_to_bf16<QK>(*reinterpret_cast<const uint4*>(src + box * (kChunk * 128) + swz128(row, unit)), lo, hi);
+    const int col = 128 * box + 16 * unit;  // first bf16 column written
+    uint8_t* d = dst + (col / 64) * (kChunk * 128);
+    const int u0 = (col % 64) / 8;
+    *reinterpret_cast<uint4*>(d + swz128(row, u0)) = lo;
+    *reinterpret_cast<uint4*>(d + swz128(row, u0 + 1)) = hi;
+  }
+}
+
+template <int D, int NT, int QK>
+__global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
+    decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap) {
+  using C = DecCfg<D, QK>;
   constexpr int ROWS = 8 * NT;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared window
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
+  uint8_t* staging = smem + C::kRingBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
   uint64_t* empty = full + C::kStages;
   float* merge_ml = reinterpret_cast<float*>(empty + C::kStages);  // [consumers][ROWS][2]
+  float* scales = merge_ml + C::kConsumers * 16 * 2;                // [stages][32] (8-bit caches)
   float* merge_o = reinterpret_cast<float*>(smem);                 // aliases the ring after the loop
   __shared__ int s_timeout;
   __shared__ int s_issued;
@@ -203,35 +263,57 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
   __syncthreads();
 
   if (warp == C::kConsumers) {
-    // ---------------- producer: page-table walk + TMA
-    if (lane == 0 && n_mine > 0) {
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
+    // ---------------- producer: page-table walk + TMA (and, for 8-bit caches, the scales)
+    if (n_mine > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+      }
       const int32_t* table = p.block_tables + (size_t)u.table_row * p.max_blocks;
       int issued = 0;
       for (int i = 0; i < n_mine; ++i) {
         const int stage = i % C::kStages;
-        if (i >= C::kStages && !mbar_wait(&empty[stage], ((i / C::kStages) - 1) & 1)) {
-          flag_error(p.err, PA_ERRBIT_WAIT_TIMEOUT);
-          atomicExch(&s_timeout, 1);
+        bool ok = true;
+        if (i >= C::kStages) ok = mbar_wait(&empty[stage], ((i / C::kStages) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) {
+            flag_error(p.err, PA_ERRBIT_WAIT_TIMEOUT);
+            atomicExch(&s_timeout, 1);
+          }
           break;
         }
         const int tok = (c_begin + i) * kChunk;
         const int page_idx = tok / p.block_size;
         const int in_page = tok - page_idx * p.block_size;
         const int page = table[page_idx];
-        if (page < 0 || page >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // TMA reads zeros
-        uint8_t* st = smem + stage * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        const bool page_ok = page >= 0 && page < p.num_blocks;
+        if constexpr (QK != 0) {
+          // lanes 0-15: the chunk's key scales, 16-31: its value scales; positions past the
+          // sequence end (or on a page outside the pool) get 0, never a stale slot's value
+          const int t = lane & 15;
+          float sc = 0.f;
+          if (page_ok && tok + t < u.len) {
+            const size_t at = ((size_t)page * p.block_size + in_page + t) * p.num_kv_heads + kvh;
+            sc = lane < 16 ? p.k_scales[at] : p.v_scales[at];
+          }
+          scales[stage * 32 + lane] = sc;
+          __syncwarp();
+        }
+        if (lane == 0) {
+          if (!page_ok) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // TMA reads zeros
+          uint8_t* st = smem + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
 #pragma unroll
-        for (int a = 0; a < C::kDChunks; ++a)
-          tma_load_4d(st + a * (kChunk * 128), &kmap, &full[stage], a * 64, kvh, in_page, page);
+          for (int a = 0; a < C::kBoxes; ++a)
+            tma_load_4d(st + a * (kChunk * 128), &kmap, &full[stage], a * (128 / C::kElt), kvh, in_page, page);
 #pragma unroll
-        for (int a = 0; a < C::kDChunks; ++a)
-          tma_load_4d(st + C::kTileBytes + a * (kChunk * 128), &vmap, &full[stage], a * 64, kvh, in_page, page);
+          for (int a = 0; a < C::kBoxes; ++a)
+            tma_load_4d(st + C::kTileBytes + a * (kChunk * 128), &vmap, &full[stage], a * (128 / C::kElt), kvh,
+                        in_page, page);
+        }
         issued = i + 1;
       }
-      s_issued = issued;
+      if (lane == 0) s_issued = issued;
     }
   } else {
     // ---------------- consumers
@@ -268,6 +350,8 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
     const int mi = lane >> 3, ri = lane & 7;
     const int k_key = ri + 8 * (mi & 1), k_unit = mi >> 1;  // K: (keys 0-7|8-15) x (unit u0|u0+1)
     const int v_key = ri + 8 * (mi >> 1), v_unit = mi & 1;  // V^T: (d 0-7|8-15) x (keys 0-7|8-15)
+    uint8_t* my_stage_k = staging + warp * (2 * kChunk * D * 2);
+    uint8_t* my_stage_v = my_stage_k + kChunk * D * 2;
 
     for (int i = warp; i < n_mine; i += C::kConsumers) {
       const int stage = i % C::kStages;
@@ -281,7 +365,20 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
       const int key0 = (c_begin + i) * kChunk;
       const int nvalid = min(kChunk, u.len - key0);
       const int nlow = u.start - key0;  // keys below this index of the chunk are outside the window
-      if (nvalid < kChunk) {
+      float ks_a = 1.f, ks_b = 1.f, vs_a = 1.f, vs_b = 1.f;
+      if constexpr (QK != 0) {
+        const float* sc = scales + stage * 32;
+        ks_a = sc[g4];
+        ks_b = sc[g4 + 8];
+        vs_a = sc[16 + g4];
+        vs_b = sc[16 + g4 + 8];
+        convert_tile<D, QK>(kt, my_stage_k, kChunk, lane);
+        convert_tile<D, QK>(vt, my_stage_v, nvalid, lane);  // rows past the end become zeros
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);  // the codes are no longer needed
+        kt = my_stage_k;
+        vt = my_stage_v;
+      } else if (nvalid < kChunk) {
         // rows past the sequence end may hold anything (NaN included): zero them so that
         // 0-probability keys contribute exactly 0 to P.V (a select, not a multiply)
         for (int idx = lane; idx < (kChunk - nvalid) * C::kDChunks * 8; idx += 32) {
@@ -310,6 +407,12 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
+        if constexpr (QK != 0) {  // a key's scale multiplies its scores
+          s[nt][0] *= ks_a;
+          s[nt][1] *= ks_a;
+          s[nt][2] *= ks_b;
+          s[nt][3] *= ks_b;
+        }
         float x0, x1, x2, x3;
         if (p.softcap_log2 > 0.f) {
           x0 = score_log2(p, s[nt][0]);
@@ -343,8 +446,9 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
           o[nt][mt][2] *= al0;
           o[nt][mt][3] *= al1;
         }
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
+        // a value's scale multiplies its probabilities before P.V (the sums above stay unscaled)
+        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0 * vs_a, p1 * vs_a));  // keys 0-7
+        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2 * vs_b, p3 * vs_b));  // keys 8-15
       }
       // O^T[d x rows] += V^T . P^T
 #pragma unroll
@@ -356,8 +460,10 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::kThreads)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      __syncwarp();  // the staging tile (8-bit caches) is rewritten next iteration
+      if constexpr (QK == 0) {
+        if (lane == 0) mbar_arrive(&empty[stage]);
+      }
     }
     // full row sums: the 8 threads of a row each hold a share of l
 #pragma unroll
@@ -578,11 +684,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   }
 }
 
-template <int D, int NT>
-cudaError_t launch_bf16_impl(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             cudaStream_t stream) {
-  using C = Bf16Cfg<D>;
-  auto kern = decode_bf16_kernel<D, NT>;
+template <int D, int NT, int QK>
+cudaError_t launch_tc_impl(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream) {
+  using C = DecCfg<D, QK>;
+  auto kern = decode_tc_kernel<D, NT, QK>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -596,10 +702,10 @@ cudaError_t launch_bf16_impl(const DecodeParams& p, const CUtensorMap& kmap, con
   return cudaGetLastError();
 }
 
-template <int D, int NT>
-int occupancy_bf16() {
-  using C = Bf16Cfg<D>;
-  auto kern = decode_bf16_kernel<D, NT>;
+template <int D, int NT, int QK>
+int occupancy_tc() {
+  using C = DecCfg<D, QK>;
+  auto kern = decode_tc_kernel<D, NT, QK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return 1;
   int n = 0;
@@ -640,23 +746,34 @@ int pad_group(int g) {
 
 }  // namespace
 
+#define PA_TC_NT(D, QK) \
+  (p.group > 8 ? launch_tc_impl<D, 2, QK>(p, kmap, vmap, stream) : launch_tc_impl<D, 1, QK>(p, kmap, vmap, stream))
+
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream) {
-  const bool two = p.group > 8;
-  switch (p.head_dim) {
-    case 64: return two ? launch_bf16_impl<64, 2>(p, kmap, vmap, stream) : launch_bf16_impl<64, 1>(p, kmap, vmap, stream);
-    case 128: return two ? launch_bf16_impl<128, 2>(p, kmap, vmap, stream) : launch_bf16_impl<128, 1>(p, kmap, vmap, stream);
-    case 256: return two ? launch_bf16_impl<256, 2>(p, kmap, vmap, stream) : launch_bf16_impl<256, 1>(p, kmap, vmap, stream);
+  switch (p.quant * 1000 + p.head_dim) {
+    case 64: return PA_TC_NT(64, 0);
+    case 128: return PA_TC_NT(128, 0);
+    case 256: return PA_TC_NT(256, 0);
+    case 1128: return PA_TC_NT(128, 1);
+    case 1256: return PA_TC_NT(256, 1);
+    case 2128: return PA_TC_NT(128, 2);
+    case 2256: return PA_TC_NT(256, 2);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int decode_bf16_ctas_per_sm(int head_dim, int group) {
-  const bool two = group > 8;
-  switch (head_dim) {
-    case 64: return two ? occupancy_bf16<64, 2>() : occupancy_bf16<64, 1>();
-    case 128: return two ? occupancy_bf16<128, 2>() : occupancy_bf16<128, 1>();
-    case 256: return two ? occupancy_bf16<256, 2>() : occupancy_bf16<256, 1>();
+#define PA_TC_OCC(D, QK) (group > 8 ? occupancy_tc<D, 2, QK>() : occupancy_tc<D, 1, QK>())
+
+int decode_bf16_ctas_per_sm(int head_dim, int group, int quant) {
+  switch (quant * 1000 + head_dim) {
+    case 64: return PA_TC_OCC(64, 0);
+    case 128: return PA_TC_OCC(128, 0);
+    case 256: return PA_TC_OCC(256, 0);
+    case 1128: return PA_TC_OCC(128, 1);
+    case 1256: return PA_TC_OCC(256, 1);
+    case 2128: return PA_TC_OCC(128, 2);
+    case 2256: return PA_TC_OCC(256, 2);
     default: return 1;
   }
 }

@@ -31,16 +31,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// [num_blocks, block_size, Hkv, D] bf16 pool viewed as a 4-D tensor (D, Hkv, bs, blocks);
-// one box is `box_tokens` rows of one KV head, 64 columns (128 bytes, swizzled).
-bool encode_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs, int num_blocks, int box_tokens) {
+// [num_blocks, block_size, Hkv, D] pool (bf16, or 8-bit codes when elt == 1) viewed as a 4-D
+// tensor (D, Hkv, bs, blocks); one box is `box_tokens` rows of one KV head, 128 bytes wide
+// (64 bf16 or 128 codes), 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs, int num_blocks, int box_tokens,
+                      int elt = 2) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)bs, (cuuint64_t)num_blocks};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)bs * Hkv * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tokens, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)D * elt, (cuuint64_t)Hkv * D * elt, (cuuint64_t)bs * Hkv * D * elt};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 1, (cuuint32_t)box_tokens, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = enc(map, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                   const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -62,7 +65,7 @@ bool encode_query_map(CUtensorMap* map, const void* base, int D, int Hq, int N, 
 
 struct DeviceInfo {
   int sms = 0;
-  int occ_bf16[3][2] = {};  // [D 64/128/256][group <= 8 | > 8]
+  int occ_bf16[3][3][2] = {};  // [bf16 | int8 | fp8][D 64/128/256][group <= 8 | > 8]
   int occ_f32[3][5] = {};   // [D][padded group 1..16]
 };
 
@@ -201,11 +204,12 @@ pa_status validate_common(const void* q, const void* k_cache, const void* v_cach
   return PA_OK;
 }
 
-int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long max_chunks, pa_dtype dtype) {
+int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long max_chunks, pa_dtype dtype,
+                int quant = 0) {
   int occ;
-  if (dtype == PA_DTYPE_BF16) {
-    int& slot = info->occ_bf16[dim_index(D)][G > 8 ? 1 : 0];
-    if (slot == 0) slot = decode_bf16_ctas_per_sm(D, G);
+  if (dtype == PA_DTYPE_BF16 || quant != 0) {
+    int& slot = info->occ_bf16[quant][dim_index(D)][G > 8 ? 1 : 0];
+    if (slot == 0) slot = decode_bf16_ctas_per_sm(D, G, quant);
     occ = slot;
   } else {
     int& slot = info->occ_f32[dim_index(D)][log2i(G)];
@@ -227,7 +231,7 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   const int D = p.head_dim;
   const long long max_chunks = cdivll((long long)p.max_blocks * p.block_size, kChunk);
   int splits = requested_splits;
-  if (splits <= 0) splits = auto_splits(info, p.num_units, p.num_kv_heads, D, p.group, max_chunks, dtype);
+  if (splits <= 0) splits = auto_splits(info, p.num_units, p.num_kv_heads, D, p.group, max_chunks, dtype, p.quant);
   splits = (int)std::min<long long>(splits, max_chunks);
   const int per = (int)cdivll(max_chunks, splits);
   splits = (int)cdivll(max_chunks, per);
@@ -241,10 +245,11 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
     p.ws_ml = p.ws_acc + (size_t)p.num_units * splits * p.num_q_heads * D;
   }
   cudaError_t e;
-  if (dtype == PA_DTYPE_BF16) {
+  if (dtype == PA_DTYPE_BF16 || p.quant != 0) {
+    const int elt = p.quant != 0 ? 1 : 2;
     CUtensorMap kmap, vmap;
-    if (!encode_cache_map(&kmap, k_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk) ||
-        !encode_cache_map(&vmap, v_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk))
+    if (!encode_cache_map(&kmap, k_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk, elt) ||
+        !encode_cache_map(&vmap, v_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk, elt))
       return PA_ERR_CUDA;
     e = launch_decode_bf16(p, kmap, vmap, stream);
   } else {
@@ -252,7 +257,7 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (splits > 1) {
-    e = launch_combine(p, dtype, stream);
+    e = launch_combine(p, p.quant != 0 ? PA_DTYPE_BF16 : dtype, stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
@@ -438,4 +443,139 @@ extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_c
   st = apply_options(options, sc, p);
   if (st != PA_OK) return st;
   return run_decode_units(p, dtype, k_cache, v_cache, 1, nullptr, 0, s);
+}
+
+// ------------------------------------------------------------------------------ 8-bit caches
+namespace {
+
+int quant_kind(pa_dtype cache_dtype) {
+  return cache_dtype == PA_DTYPE_INT8 ? 1 : (cache_dtype == PA_DTYPE_FP8_E4M3 ? 2 : 0);
+}
+
+// Shapes the 8-bit paths serve: bf16 queries, D 128 or 256 (a cached row spans whole 128-byte
+// columns), groups up to 16, 16-token chunks.
+pa_status validate_quant(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
+                         const float* v_scales, pa_dtype cache_dtype, const int32_t* block_tables, const void* out,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         int max_blocks_per_seq, float scale) {
+  if (!k_scales || !v_scales) return PA_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u))
+    return PA_ERR_INVALID_ARGUMENT;
+  pa_status st = validate_common(q, k_cache, v_cache, block_tables, out, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, num_blocks, max_blocks_per_seq, scale, PA_DTYPE_BF16);
+  if (st != PA_OK) return st;
+  if (quant_kind(cache_dtype) == 0) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_reshape_and_cache_quant(const void* key, const void* value, pa_dtype src_dtype,
+                                                void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                                pa_dtype cache_dtype, const int32_t* slot_mapping, int num_tokens,
+                                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                                int32_t* error_word, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (src_dtype != PA_DTYPE_BF16 && src_dtype != PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
+  if (quant_kind(cache_dtype) == 0) return PA_ERR_UNSUPPORTED;
+  if (head_dim % 32 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !k_scales || !v_scales || !slot_mapping)
+    return PA_ERR_INVALID_ARGUMENT;
+  cudaError_t e = launch_reshape_and_cache_quant(key, value, src_dtype == PA_DTYPE_BF16, k_cache, v_cache, k_scales,
+                                                 v_scales, cache_dtype == PA_DTYPE_FP8_E4M3, slot_mapping, num_tokens,
+                                                 num_kv_heads, head_dim, (long long)num_blocks * block_size,
+                                                 error_word, as_stream(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_paged_attention_decode_quant(const void* q, const void* k_cache, const void* v_cache,
+                                                     const float* k_scales, const float* v_scales,
+                                                     pa_dtype cache_dtype, const int32_t* block_tables,
+                                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                                     int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                                     int max_blocks_per_seq, float scale, int num_splits, void* out,
+                                                     void* workspace, size_t workspace_bytes,
+                                                     const pa_attn_options* options, int32_t* error_word,
+                                                     void* stream) {
+  if (num_seqs < 0 || num_splits < 0 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0) return PA_OK;
+  if (!context_lens) return PA_ERR_INVALID_ARGUMENT;
+  pa_status st = validate_quant(q, k_cache, v_cache, k_scales, v_scales, cache_dtype, block_tables, out, num_q_heads,
+                                num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  if (st != PA_OK) return st;
+  if ((long long)num_seqs * num_kv_heads * kMaxSplits > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = error_word;
+  p.num_units = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.quant = quant_kind(cache_dtype);
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+  p.scale_log2 = sc * kLog2e;
+  st = apply_options(options, sc, p);
+  if (st != PA_OK) return st;
+  return run_decode_units(p, PA_DTYPE_BF16, k_cache, v_cache, num_splits, workspace, workspace_bytes,
+                          as_stream(stream));
+}
+
+extern "C" pa_status pa_paged_attention_varlen_quant(const void* q, const void* k_cache, const void* v_cache,
+                                                     const float* k_scales, const float* v_scales,
+                                                     pa_dtype cache_dtype, const int32_t* query_start_loc,
+                                                     const int32_t* seq_lens, const int32_t* block_tables,
+                                                     int num_reqs, int num_tokens, int max_query_len,
+                                                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                                     int num_blocks, int max_blocks_per_seq, int causal, float scale,
+                                                     void* out, const pa_attn_options* options, int32_t* error_word,
+                                                     void* stream) {
+  if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
+  if (num_reqs == 0 || num_tokens == 0) return PA_OK;
+  if (!query_start_loc || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
+  pa_status st = validate_quant(q, k_cache, v_cache, k_scales, v_scales, cache_dtype, block_tables, out, num_q_heads,
+                                num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  if (st != PA_OK) return st;
+  if ((long long)num_tokens * num_kv_heads > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.query_start_loc = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.err = error_word;
+  p.varlen = 1;
+  p.causal = causal ? 1 : 0;
+  p.num_reqs = num_reqs;
+  p.num_units = num_tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.quant = quant_kind(cache_dtype);
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+  p.scale_log2 = sc * kLog2e;
+  st = apply_options(options, sc, p);
+  if (st != PA_OK) return st;
+  return run_decode_units(p, PA_DTYPE_BF16, k_cache, v_cache, 1, nullptr, 0, as_stream(stream));
 }

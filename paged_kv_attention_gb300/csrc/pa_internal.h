@@ -47,16 +47,25 @@ struct DecodeParams {
   float softcap_log2;    // > 0: score -> softcap * tanh(scale * s / softcap), in log2 units (* log2 e)
   float scale_over_cap;  // scale / softcap
   const float* sinks;    // nullable [Hq]: per-head sink logit (natural-log units)
+  // 8-bit caches: 0 = bf16 values, 1 = int8 codes, 2 = fp8 E4M3 codes; scales [blocks, bs, Hkv]
+  int quant;
+  const float* k_scales;
+  const float* v_scales;
 };
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                      const int32_t* slot_mapping, int num_tokens, int row_bytes,
                                      long long num_slots, int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_reshape_and_cache_quant(const void* key, const void* value, bool src_bf16, void* k_cache,
+                                           void* v_cache, float* k_scales, float* v_scales, bool fp8,
+                                           const int32_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                           int head_dim, long long num_slots, int32_t* err, cudaStream_t stream);
+
 // bf16 tensor-core decode (TMA page loads, mma.sync, 16-token chunks).
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream);
-int decode_bf16_ctas_per_sm(int head_dim, int group);
+int decode_bf16_ctas_per_sm(int head_dim, int group, int quant);
 
 // fp32 CUDA-core decode.
 cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream);

@@ -1,0 +1,111 @@
+"""GPU parity of the 8-bit KV cache: the quantising write is bit-exact against the oracle's
+quantiser (same float32 arithmetic), and decode / varlen over int8 and fp8 pools match the
+float64 attention over the oracle's dequantised cache within the bf16 tolerance."""
+
+import pytest
+import torch
+
+import paged_kv_attention_gb300 as pa
+import workloads
+from oracle import quant
+from paged_helpers import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+KINDS = {"int8": torch.int8, "fp8": torch.float8_e4m3fn}
+
+
+def pools(case, kind, dev):
+    shape = (case.num_blocks, case.block_size, case.num_kv_heads, case.head_dim)
+    kc = torch.zeros(shape, dtype=KINDS[kind], device=dev)
+    vc = torch.zeros(shape, dtype=KINDS[kind], device=dev)
+    # scales of unwritten slots are NaN: a kernel that reads one shows it
+    ks = torch.full(shape[:3], float("nan"), dtype=torch.float32, device=dev)
+    vs = torch.full(shape[:3], float("nan"), dtype=torch.float32, device=dev)
+    return kc, vc, ks, vs
+
+
+def filled(case, kind):
+    g = pools(case, kind, DEV)
+    pa.reshape_and_cache_quant(case.key.to(DEV), case.value.to(DEV), *g, case.slot_mapping.to(DEV))
+    o = pools(case, kind, "cpu")
+    quant.reshape_and_cache_quant(case.key, case.value, *o, case.slot_mapping, kind)
+    return g, o
+
+
+def _bits(t):
+    return t.view(torch.uint8) if t.element_size() == 1 else t.view(torch.int32)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("src", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("hkv,d", [(8, 128), (4, 256), (2, 64)])
+def test_quantizing_write_is_bit_exact(kind, src, hkv, d):
+    case = workloads.make_case("qw", 700 + d, [1, 1, 1], [37, 300, 5], num_q_heads=hkv, num_kv_heads=hkv,
+                               head_dim=d, block_size=16, dtype=src)
+    slots = case.slot_mapping.clone()
+    slots[::9] = -1
+    case.slot_mapping = slots
+    g, o = filled(case, kind)
+    torch.cuda.synchronize()
+    for a, b in zip(g, o):
+        assert torch.equal(_bits(a.cpu()), _bits(b))
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("head_dim,hq,hkv", [(128, 32, 8), (256, 16, 4), (128, 16, 1), (128, 8, 8)])
+@pytest.mark.parametrize("splits", [1, 4, 0])
+def test_decode(kind, head_dim, hq, hkv, splits):
+    case = workloads.decode_case("qd", 710 + head_dim + hq, [1, 15, 16, 17, 300, 2049], num_q_heads=hq,
+                                 num_kv_heads=hkv, head_dim=head_dim, block_size=16, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    out = pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                          case.seq_lens.to(DEV), case.scale, num_splits=splits)
+    want = quant.paged_attention_decode_quant(case.q, ko, vo, kso, vso, case.block_tables, case.seq_lens, case.scale)
+    check_close(out, want, torch.bfloat16, label=f"{kind} D{head_dim} G{hq // hkv} splits={splits}")
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_decode_with_modifiers(kind):
+    case = workloads.decode_case("qm", 720, [40, 333, 1500], num_q_heads=16, num_kv_heads=4, head_dim=128,
+                                 block_size=32, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    sinks = torch.randn(16, generator=torch.Generator().manual_seed(1))
+    out = pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                          case.seq_lens.to(DEV), case.scale, window=100, softcap=4.0,
+                                          sinks=sinks.to(DEV))
+    want = quant.paged_attention_decode_quant(case.q, ko, vo, kso, vso, case.block_tables, case.seq_lens, case.scale,
+                                              window=100, softcap=4.0, sinks=sinks.double())
+    check_close(out, want, torch.bfloat16, label=f"{kind} modifiers")
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_varlen(kind):
+    case = workloads.make_case("qv", 730, [37, 1, 5, 0, 64], [90, 33, 64, 12, 64], num_q_heads=32, num_kv_heads=8,
+                               head_dim=128, block_size=16, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    out = pa.paged_attention_varlen_quant(case.q.to(DEV), kc, vc, ks, vs, case.query_start_loc.to(DEV),
+                                          case.seq_lens.to(DEV), case.block_tables.to(DEV), case.max_query_len,
+                                          True, case.scale)
+    want = quant.paged_attention_varlen_quant(case.q, ko, vo, kso, vso, case.query_start_loc, case.seq_lens,
+                                              case.block_tables, True, case.scale)
+    check_close(out, want, torch.bfloat16, label=f"{kind} varlen")
+
+
+def test_64x4096_int8_decode_full_size():
+    case = workloads.NAMED["decode_64x4096_bf16"]()
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, "int8")
+    out = pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                          case.seq_lens.to(DEV), case.scale)
+    want = quant.paged_attention_decode_quant(case.q, ko, vo, kso, vso, case.block_tables, case.seq_lens, case.scale)
+    check_close(out, want, torch.bfloat16, label="int8 64x4096")
+
+
+def test_unsupported_head_dim_is_refused():
+    case = workloads.decode_case("qx", 740, [10], num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                                 dtype=torch.bfloat16)
+    (kc, vc, ks, vs), _ = filled(case, "int8")
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                        case.seq_lens.to(DEV), case.scale)
+    assert e.value.status == pa._lib.PA_ERR_UNSUPPORTED
