@@ -382,6 +382,56 @@ def decode_leg(args, world, rank, dev):
                 launches=args.steps * (2 + (1 if splits > 1 else 0)))
 
 
+def decode_int8_leg(args, dev):
+    """The same 64x4096 decode over an int8 cache (codes + one fp32 scale per (slot, KV head)),
+    quantised by the library's own write; the decode call replayed as a CUDA graph."""
+    import paged_kv_attention_gb300 as pa
+    import workloads
+    case = workloads.NAMED[DECODE_WORKLOAD]()
+    if args.decode_seqs != case.num_reqs:  # a smaller batch of the same workload (profiling)
+        case = workloads.decode_case(f"decode_{args.decode_seqs}x4096_bf16", 1003, [4096] * args.decode_seqs,
+                                     num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                     dtype=torch.bfloat16)
+    S, Hq, Hkv, D, bs = case.num_reqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
+    shape = (case.num_blocks, bs, Hkv, D)
+    kc = torch.empty(shape, dtype=torch.int8, device=dev)
+    vc = torch.empty(shape, dtype=torch.int8, device=dev)
+    ks = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    vs = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    pa.reshape_and_cache_quant(case.key.to(dev), case.value.to(dev), kc, vc, ks, vs, case.slot_mapping.to(dev))
+    q, tables, ctx = case.q.to(dev), case.block_tables.to(dev), case.seq_lens.to(dev)
+    out = torch.empty_like(q)
+    splits = pa.decode_auto_splits(S, Hq, Hkv, D, bs, tables.shape[1], torch.bfloat16)
+    ws = torch.empty(max(pa.decode_workspace_bytes(S, Hq, D, tables.shape[1], bs, 0), 16), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        pa.paged_attention_decode_quant(q, kc, vc, ks, vs, tables, ctx, case.scale, out=out, workspace=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(3):
+        g.replay()
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    lens = case.seq_lens.tolist()
+    positions = sum(int(L) for L in lens)
+    nbytes = positions * Hkv * (2 * D * 1 + 2 * 4) + 2 * S * Hq * D * 2 + \
+        sum(-(-int(L) // bs) for L in lens) * 4 + S * 4
+    return dict(ms=ms, bytes=nbytes, gbs=nbytes / (ms / 1e3) / 1e9)
+
+
 def prefill_leg(args, dev, steps):
     import paged_kv_attention_gb300 as pa
     import workloads
@@ -430,12 +480,13 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "int8"], default="all",
                     help="run one leg only (profiling runs)")
     ap.add_argument("--decode-seqs", type=int, default=64, help="sequences of 4096 tokens in the decode leg")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the decode step eagerly, not as CUDA graphs")
+    ap.add_argument("--no-int8", action="store_true", help="skip the int8-cache decode leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -450,9 +501,16 @@ def main():
     peaks, peak_src = load_peaks()
     traffic = load_traffic()
 
+    if args.only == "int8":
+        q8 = decode_int8_leg(args, dev)
+        if rank == 0:
+            print(json.dumps({"int8_only": True, "value": round(q8["gbs"], 2), "unit": "GB/s",
+                              "call_ms": round(q8["ms"], 5)}), flush=True)
+        return
     with ClockSampler(local) as clocks:
         d = None if args.only == "prefill" else decode_leg(args, world, rank, dev)
         p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps)
+        q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
     clk = clocks.summary()
     if d is None:
         if rank == 0 and p is not None:
@@ -506,6 +564,12 @@ def main():
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": round(p["tflops"] / tf_peak, 4),
                          "peak_source": peak_src, "traffic": traffic.get("varlen_kernel")},
         }
+    if q8 is not None:
+        line["decode_int8"] = {
+            "workload": "decode_64x4096_int8 (same queries and tokens, int8 codes + fp32 scales)",
+            "value": round(q8["gbs"], 2), "unit": "GB/s", "call_ms": round(q8["ms"], 5),
+            "algorithmic_bytes_per_launch": q8["bytes"], "frac_of_hbm_peak": round(q8["gbs"] / hbm, 4),
+            "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and case.num_reqs == 64:
         _, ko_vo = None, oracle_pools(case)
         v, dt, n, threads = time_oracle_decode(case, *ko_vo)

@@ -144,6 +144,18 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_16816_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// bf16 operands for bf16 caches, fp16 for converted 8-bit codes
+template <int QK>
+__device__ __forceinline__ void mma_cache(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (QK == 0) mma_16816(c, a, b0, b1); else mma_16816_f16(c, a, b0, b1);
+}
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -151,10 +163,13 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // QK selects the cache format: 0 = bf16 values; 1 = int8 codes, 2 = fp8 E4M3 codes, each with
-// one fp32 scale per (slot, KV head). 8-bit codes are converted to bf16 in shared memory (exact:
-// |code| <= 127, and every E4M3 value is a bf16 value); the key's scale multiplies its scores
-// and the value's scale its probabilities before P.V ("TileInfer.jl - Attention kernels",
-// INT8 cache).
+// one fp32 scale per (slot, KV head). 8-bit codes are converted exactly to 16-bit values in
+// shared memory; the key's scale multiplies its scores and the value's scale its probabilities
+// before P.V ("TileInfer.jl - Attention kernels", INT8 cache). The page converts to bf16; here
+// the 16-bit type is fp16, which holds every code exactly and converts from int8 in about one
+// instruction per code (from bf16 it would take three), so the MMAs for 8-bit caches run in fp16
+// with fp32 accumulation, the queries converted once per CTA (exact within fp16's range) and the
+// probabilities rounded to fp16 (3 more mantissa bits than bf16).
 template <int D, int QK>
 struct DecCfg {
   static constexpr int kConsumers = 4;
@@ -164,46 +179,69 @@ struct DecCfg {
   static constexpr int kDChunks = D / 64;                // 128-byte columns of a bf16 row
   static constexpr int kTileBytes = kChunk * D * kElt;   // K or V rows of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = 65536 / kStageBytes;    // 64 KiB ring
+  static constexpr int kStages = (QK ? 32768 : 65536) / kStageBytes;  // 64 KiB ring (32 KiB for codes)
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMT = D / 16;
-  static constexpr int kStagingBytes = QK ? kConsumers * 2 * kChunk * D * 2 : 0;  // bf16 K and V per consumer
+  // bf16 staging of converted codes: per consumer a K and a V tile of kDChunks column halves,
+  // each half 16 bytes further than a plain 2 KiB step so the conversion's stores to the two
+  // halves of one row fall on different banks (the swizzle is applied per row, so reads are
+  // unaffected)
+  static constexpr int kStageRegion = kChunk * 128 + 16;
+  static constexpr int kStagingTile = ((D / 64) * kStageRegion + 127) / 128 * 128;
+  static constexpr int kStagingBytes = QK ? kConsumers * 2 * kStagingTile : 0;
   static constexpr int kScaleBytes = QK ? kStages * 32 * 4 : 0;                   // 16 K + 16 V scales per stage
   // ring | staging | full, empty barriers | merge (m, l) | scales; the merge accumulators alias the ring
   static constexpr int kSmemBytes =
       1024 + kRingBytes + kStagingBytes + 2 * kStages * 8 + kConsumers * 16 * 2 * 4 + kScaleBytes;
   static_assert(kBoxes >= 1, "a cached row must span at least one 128-byte column");
   static_assert(kStages % kConsumers == 0, "stages are dealt to consumers round robin");
-  static_assert(kConsumers * 16 * D * 4 <= kRingBytes, "merge area must fit in the ring");
+  static_assert(kConsumers * 16 * D * 4 <= kRingBytes + kStagingBytes, "merge area must fit in ring + staging");
 };
 
-// 16 codes (one 16-byte unit) -> 16 bf16 (two 16-byte units), exactly.
+// 16 codes (one 16-byte unit) -> 16 fp16 (two 16-byte units), exactly (|int8 code| <= 128 and
+// every E4M3 value are fp16 values).
 template <int QK>
-__device__ __forceinline__ void codes_to_bf16(uint4 raw, uint4& lo, uint4& hi) {
+__device__ __forceinline__ void codes_to_f16(uint4 raw, uint4& lo, uint4& hi) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   uint32_t o[8];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (QK == 1) {
-      const float f0 = (float)(int8_t)(w[k] & 0xffu), f1 = (float)(int8_t)((w[k] >> 8) & 0xffu);
-      const float f2 = (float)(int8_t)((w[k] >> 16) & 0xffu), f3 = (float)(int8_t)(w[k] >> 24);
-      o[2 * k] = pack_bf16x2(f0, f1);
-      o[2 * k + 1] = pack_bf16x2(f2, f3);
+      // code c -> byte b = c + 128; the fp16 with bits 0x64bb is 1024 + b, so subtracting
+      // 1152 gives c exactly: two byte permutes and two packed subtractions per four codes
+      const uint32_t y = w[k] ^ 0x80808080u;
+      const uint32_t h01 = __byte_perm(y, 0x64646464u, 0x5140);
+      const uint32_t h23 = __byte_perm(y, 0x64646464u, 0x5342);
+      const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+      const __half2 c01 = __hsub2(*reinterpret_cast<const __half2*>(&h01), bias);
+      const __half2 c23 = __hsub2(*reinterpret_cast<const __half2*>(&h23), bias);
+      o[2 * k] = *reinterpret_cast<const uint32_t*>(&c01);
+      o[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&c23);
     } else {
       const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] & 0xffffu), __NV_E4M3);
       const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] >> 16), __NV_E4M3);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-      o[2 * k] = pack_bf16x2(a.x, a.y);
-      o[2 * k + 1] = pack_bf16x2(b.x, b.y);
+      o[2 * k] = (uint32_t)h01.x | ((uint32_t)h01.y << 16);
+      o[2 * k + 1] = (uint32_t)h23.x | ((uint32_t)h23.y << 16);
     }
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// A 16-row tile of codes (kBoxes swizzled 128-byte columns) -> the bf16 tile layout the MMA
-// path reads (kDChunks swizzled 128-byte columns). Rows at or past `valid_rows` become zeros.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low half)
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// bf16 pair -> fp16 pair (exact within fp16's range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+  return pack_f16x2(lo, hi);
+}
+
+// A 16-row tile of codes (kBoxes swizzled 128-byte columns) -> the 16-bit tile layout the MMA
+// path reads (kDChunks swizzled 128-byte columns), in fp16. Rows at or past `valid_rows` become
+// zeros.
 template <int D, int QK>
 __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int valid_rows, int lane) {
   using C = DecCfg<D, QK>;
@@ -212,9 +250,9 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
     const int rest = idx - row * (C::kBoxes * 8);
     const int box = rest >> 3, unit = rest & 7;  // codes 128 * box + 16 * unit .. + 15
     uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-    if (row < valid_rows) codes_to_bf16<QK>(*reinterpret_cast<const uint4*>(src + box * (kChunk * 128) + swz128(row, unit)), lo, hi);
+    if (row < valid_rows) codes_to_f16<QK>(*reinterpret_cast<const uint4*>(src + box * (kChunk * 128) + swz128(row, unit)), lo, hi);
     const int col = 128 * box + 16 * unit;  // first bf16 column written
-    uint8_t* d = dst + (col / 64) * (kChunk * 128);
+    uint8_t* d = dst + (col / 64) * C::kStageRegion;
     const int u0 = (col % 64) / 8;
     *reinterpret_cast<uint4*>(d + swz128(row, u0)) = lo;
     *reinterpret_cast<uint4*>(d + swz128(row, u0 + 1)) = hi;
@@ -253,7 +291,8 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
+      // 8-bit caches: the 32 scale copies of a stage arrive on its barrier too
+      mbar_init(&full[i], QK != 0 ? 33 : 1);
       mbar_init(&empty[i], 1);
     }
     fence_barrier_init();
@@ -270,6 +309,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         prefetch_tensormap(&vmap);
       }
       const int32_t* table = p.block_tables + (size_t)u.table_row * p.max_blocks;
+      // page ids are fetched 32 at a time, one per lane, and handed out by shuffle: one
+      // table-load latency per 32 pages instead of one per chunk
+      int win_base = -64, my_page = -1;
       int issued = 0;
       for (int i = 0; i < n_mine; ++i) {
         const int stage = i % C::kStages;
@@ -285,19 +327,25 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         const int tok = (c_begin + i) * kChunk;
         const int page_idx = tok / p.block_size;
         const int in_page = tok - page_idx * p.block_size;
-        const int page = table[page_idx];
+        if (page_idx - win_base >= 32) {  // uniform: every lane has the same page_idx
+          win_base = page_idx;
+          my_page = (win_base + lane < p.max_blocks) ? __ldg(table + win_base + lane) : -1;
+        }
+        const int page = __shfl_sync(0xffffffffu, my_page, page_idx - win_base);
         const bool page_ok = page >= 0 && page < p.num_blocks;
         if constexpr (QK != 0) {
-          // lanes 0-15: the chunk's key scales, 16-31: its value scales; positions past the
-          // sequence end (or on a page outside the pool) get 0, never a stale slot's value
+          // lanes 0-15: the chunk's key scales, 16-31: its value scales, copied asynchronously
+          // (the producer never waits on them); positions past the sequence end, or on a page
+          // outside the pool, are zero-filled instead of read
           const int t = lane & 15;
-          float sc = 0.f;
-          if (page_ok && tok + t < u.len) {
-            const size_t at = ((size_t)page * p.block_size + in_page + t) * p.num_kv_heads + kvh;
-            sc = lane < 16 ? p.k_scales[at] : p.v_scales[at];
-          }
-          scales[stage * 32 + lane] = sc;
-          __syncwarp();
+          const bool take = page_ok && tok + t < u.len;
+          const float* base = lane < 16 ? p.k_scales : p.v_scales;
+          const float* src = take ? base + ((size_t)page * p.block_size + in_page + t) * p.num_kv_heads + kvh : base;
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(scales + stage * 32 + lane)),
+                       "l"(src), "r"(take ? 4 : 0)
+                       : "memory");
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[stage]))
+                       : "memory");
         }
         if (lane == 0) {
           if (!page_ok) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // TMA reads zeros
@@ -333,6 +381,10 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         for (int kk = 0; kk < C::kMT; ++kk) {
           qf[nt][kk][0] = (n < G) ? __ldg(qr + (kk * 16 + 2 * t4) / 2) : 0u;
           qf[nt][kk][1] = (n < G) ? __ldg(qr + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
+          if constexpr (QK != 0) {  // the converted codes are fp16: so are the queries
+            qf[nt][kk][0] = bf16x2_to_f16x2(qf[nt][kk][0]);
+            qf[nt][kk][1] = bf16x2_to_f16x2(qf[nt][kk][1]);
+          }
         }
       }
     }
@@ -350,8 +402,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     const int mi = lane >> 3, ri = lane & 7;
     const int k_key = ri + 8 * (mi & 1), k_unit = mi >> 1;  // K: (keys 0-7|8-15) x (unit u0|u0+1)
     const int v_key = ri + 8 * (mi >> 1), v_unit = mi & 1;  // V^T: (d 0-7|8-15) x (keys 0-7|8-15)
-    uint8_t* my_stage_k = staging + warp * (2 * kChunk * D * 2);
-    uint8_t* my_stage_v = my_stage_k + kChunk * D * 2;
+    uint8_t* my_stage_k = staging + warp * (2 * C::kStagingTile);
+    uint8_t* my_stage_v = my_stage_k + C::kStagingTile;
+    constexpr int kRegionStride = QK ? C::kStageRegion : kChunk * 128;  // bytes between column halves
 
     for (int i = warp; i < n_mine; i += C::kConsumers) {
       const int stage = i % C::kStages;
@@ -399,9 +452,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         uint32_t a[4];
         const int dch = kk >> 2;
         const int unit_idx = 2 * (kk & 3) + k_unit;
-        ldsm_x4(a, smem_addr(kt + dch * (kChunk * 128) + swz128(k_key, unit_idx)));
+        ldsm_x4(a, smem_addr(kt + dch * kRegionStride + swz128(k_key, unit_idx)));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_cache<QK>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
       }
       // online softmax (rows 2*t4 and 2*t4+1; keys g4 and g4+8)
       uint32_t pb[NT][2];
@@ -447,8 +500,13 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
           o[nt][mt][3] *= al1;
         }
         // a value's scale multiplies its probabilities before P.V (the sums above stay unscaled)
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0 * vs_a, p1 * vs_a));  // keys 0-7
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2 * vs_b, p3 * vs_b));  // keys 8-15
+        if constexpr (QK == 0) {
+          pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
+          pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
+        } else {
+          pb[nt][0] = movmatrix_trans(pack_f16x2(p0 * vs_a, p1 * vs_a));
+          pb[nt][1] = movmatrix_trans(pack_f16x2(p2 * vs_b, p3 * vs_b));
+        }
       }
       // O^T[d x rows] += V^T . P^T
 #pragma unroll
@@ -456,9 +514,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         uint32_t a[4];
         const int dch = mt >> 2;
         const int unit_idx = 2 * (mt & 3) + v_unit;
-        ldsm_x4_trans(a, smem_addr(vt + dch * (kChunk * 128) + swz128(v_key, unit_idx)));
+        ldsm_x4_trans(a, smem_addr(vt + dch * kRegionStride + swz128(v_key, unit_idx)));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_cache<QK>(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
       __syncwarp();  // the staging tile (8-bit caches) is rewritten next iteration
       if constexpr (QK == 0) {
