@@ -237,6 +237,13 @@ pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const
                                        void* out, const pa_attn_options* options, int32_t* error_word,
                                        void* stream);
 
+/* Self-test of the bounded waits inside the kernels (failure detection without a fault): a
+ * one-thread kernel waits, with a limit of limit_us microseconds (1..1,000,000), on a barrier
+ * that nothing ever completes, then ORs PA_ERRBIT_WAIT_TIMEOUT into *error_word (a device
+ * int32) and returns, leaving the context usable. Every pipelined kernel waits through the
+ * same helper with a 2-second limit. */
+pa_status pa_selftest_wait_timeout(int limit_us, int32_t* error_word, void* stream);
+
 /* ---------------------------------------------------------------------------------------
  * 8-bit KV cache. "32. Production attention kernels", Quantized KV caches; "TileInfer.jl -
  * Attention kernels", INT8 cache. The pools hold one code per element ([num_blocks,

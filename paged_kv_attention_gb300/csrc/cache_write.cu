@@ -88,7 +88,24 @@ __global__ void __launch_bounds__(256) reshape_and_cache_quant_kernel(
   }
 }
 
+// Self-test of the bounded wait every pipelined kernel uses: one thread waits on a fresh
+// mbarrier that nothing will ever arrive at, with the given limit, and reports the expiry
+// through the error word exactly as a kernel does. No other thread waits on anything.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, int32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait(&bar, 0, limit_ns)) flag_error(err, PA_ERRBIT_WAIT_TIMEOUT);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache_quant(const void* key, const void* value, bool src_bf16, void* k_cache,
                                            void* v_cache, float* k_scales, float* v_scales, bool fp8,

@@ -579,3 +579,10 @@ extern "C" pa_status pa_paged_attention_varlen_quant(const void* q, const void* 
   if (st != PA_OK) return st;
   return run_decode_units(p, PA_DTYPE_BF16, k_cache, v_cache, 1, nullptr, 0, as_stream(stream));
 }
+
+extern "C" pa_status pa_selftest_wait_timeout(int limit_us, int32_t* error_word, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000 || error_word == nullptr) return PA_ERR_INVALID_ARGUMENT;
+  return launch_wait_timeout_selftest((uint64_t)limit_us * 1000ull, error_word, as_stream(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}

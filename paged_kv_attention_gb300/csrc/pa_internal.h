@@ -57,6 +57,8 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                                      const int32_t* slot_mapping, int num_tokens, int row_bytes,
                                      long long num_slots, int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t stream);
+
 cudaError_t launch_reshape_and_cache_quant(const void* key, const void* value, bool src_bf16, void* k_cache,
                                            void* v_cache, float* k_scales, float* v_scales, bool fp8,
                                            const int32_t* slot_mapping, int num_tokens, int num_kv_heads,

@@ -118,3 +118,32 @@ def test_query_longer_than_context_is_flagged():
     ko, vo = oracle_pools(case)
     want = oracle_varlen(case, ko, vo)
     check_close(out[4:], want[4:], torch.bfloat16, label="clean request")
+
+
+def test_cuda_graph_replay_follows_device_positions():
+    """The varlen launch shape depends on host sizes only: a captured call replays correctly
+    after seq_lens (a device buffer) grow, i.e. the queries move to later positions."""
+    full = [700, 300, 1200]
+    q_lens = [64, 1, 5]
+    case = workloads.make_case("vg", 95, q_lens, full, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    q = case.q.to(DEV)
+    qsl = case.query_start_loc.to(DEV)
+    tables = case.block_tables.to(DEV)
+    lens = torch.tensor([500, 100, 900], dtype=torch.int32, device=DEV)
+    out = torch.empty_like(q)
+    pa.paged_attention_varlen(q, kc, vc, qsl, lens, tables, 64, True, case.scale, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pa.paged_attention_varlen(q, kc, vc, qsl, lens, tables, 64, True, case.scale, out=out)
+    for step in range(3):
+        new = torch.tensor([500 + 64 * step, 100 + 90 * step, 900 + 140 * step], dtype=torch.int32)
+        lens.copy_(new.to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, new, case.block_tables, True,
+                                             case.scale)
+        check_close(out, want, torch.bfloat16, label=f"varlen graph step {step}")
