@@ -569,7 +569,7 @@ def main():
             "workload": "decode_64x4096_int8 (same queries and tokens, int8 codes + fp32 scales)",
             "value": round(q8["gbs"], 2), "unit": "GB/s", "call_ms": round(q8["ms"], 5),
             "algorithmic_bytes_per_launch": q8["bytes"], "frac_of_hbm_peak": round(q8["gbs"] / hbm, 4),
-            "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3)}
+            "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3), "traffic": traffic.get("decode_int8_kernel")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and case.num_reqs == 64:
         _, ko_vo = None, oracle_pools(case)
         v, dt, n, threads = time_oracle_decode(case, *ko_vo)
