@@ -19,6 +19,7 @@ hand-written golden fixture); no function is "parity unpinned".
 from . import quant  # noqa: F401
 from .attention import (  # noqa: F401
     attend,
+    cascade_decode,
     default_scale,
     gather_context,
     paged_attention_decode,

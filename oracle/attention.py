@@ -212,3 +212,29 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         out[idx] = attend(q.index_select(0, idx), pos, keys, values, sc, causal, window=window,
                           softcap=softcap, sinks=sinks)
     return out
+
+
+def cascade_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   prefix_table: torch.Tensor, prefix_len: int, suffix_tables: torch.Tensor,
+                   suffix_lens: torch.Tensor, scale: float | None = None) -> torch.Tensor:
+    """Decode where every sequence's context is a shared prefix followed by its own suffix.
+
+    Sequence s attends over prefix_len positions gathered from ``prefix_table`` and then
+    suffix_lens[s] positions gathered from ``suffix_tables[s]``, laid end to end; its query is
+    the last of them ("32. Production attention kernels", Long contexts: split the keys: the
+    same merge serves cascade attention, a shared prefix attended once for many requests and
+    merged with each request's own suffix). Returns [S, Hq, D] float64.
+    """
+    S, Hq, D = q.shape
+    sc = default_scale(D, scale)
+    out = torch.zeros((S, Hq, D), dtype=_F64)
+    pk = gather_context(k_cache, prefix_table, prefix_len)
+    pv = gather_context(v_cache, prefix_table, prefix_len)
+    for s in range(S):
+        length = int(suffix_lens[s])
+        keys = torch.cat([pk, gather_context(k_cache, suffix_tables[s], length)], dim=0)
+        values = torch.cat([pv, gather_context(v_cache, suffix_tables[s], length)], dim=0)
+        total = keys.shape[0]
+        pos = torch.tensor([max(total - 1, 0)], dtype=torch.long)
+        out[s] = attend(q[s:s + 1], pos, keys, values, sc, causal=False)[0]
+    return out
