@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attn HBM GB/s (% of peak) at 64x4096; prefill TFLOP/s"
 DECODE_WORKLOAD = "decode_64x4096_bf16"
 PREFILL_WORKLOAD = "prefill_4x8192_bf16"
+CASCADE_WORKLOAD = "cascade_64x4000_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -432,6 +433,73 @@ def decode_int8_leg(args, dev):
     return dict(ms=ms, bytes=nbytes, gbs=nbytes / (ms / 1e3) / 1e9)
 
 
+def cascade_leg(args, dev):
+    """64 sequences behind one shared 4,000-token prefix: the cascade decode (prefix read once,
+    suffixes split-KV, one combine) against the plain decode over each sequence's full table
+    (prefix pages + its own), both replayed as CUDA graphs. The working set of the cascade
+    (about 50 MB) fits in L2, so a 256 MB buffer is rewritten between timed calls and only the
+    calls are timed."""
+    import paged_kv_attention_gb300 as pa
+    import workloads
+    case = workloads.NAMED[CASCADE_WORKLOAD]()
+    kc, vc = (t.to(dev) for t in case.empty_pools())
+    pa.reshape_and_cache(case.key.to(dev), case.value.to(dev), kc, vc, case.slot_mapping.to(dev))
+    S, Hq, Hkv, D, bs = case.num_reqs - 1, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
+    P = int(case.seq_lens[0])
+    suffix = case.seq_lens[1:]
+    width = -(-int(suffix.max()) // bs)
+    q = case.q.to(dev)
+    ptable = case.block_tables[0].to(dev)
+    plen = torch.tensor([P], dtype=torch.int32, device=dev)
+    stables = case.block_tables[1:, :width].contiguous().to(dev)
+    slens = suffix.to(dev)
+    n_pre = -(-P // bs)
+    assert P % bs == 0, "the plain-decode comparison concatenates whole prefix pages"
+    full_tables = torch.cat([case.block_tables[0, :n_pre].expand(S, -1), case.block_tables[1:, :width]],
+                            dim=1).contiguous().to(dev)
+    full_lens = (suffix + P).to(dev)
+    out_c, out_p = torch.empty_like(q), torch.empty_like(q)
+    ws_c = torch.empty(pa._lib.load().pa_cascade_workspace_bytes(S, Hq, D, bs, ptable.numel(), width),
+                       dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(max(pa.decode_workspace_bytes(S, Hq, D, full_tables.shape[1], bs, 0), 16),
+                       dtype=torch.uint8, device=dev)
+
+    def cascade():
+        pa.cascade_decode(q, kc, vc, ptable, plen, stables, slens, case.scale, out=out_c, workspace=ws_c)
+
+    def plain():
+        pa.paged_attention_decode(q, kc, vc, full_tables, full_lens, case.scale, out=out_p, workspace=ws_p)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    result = {}
+    for name, fn in (("cascade", cascade), ("plain", plain)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(3):
+            g.replay()
+        n = max(20, min(args.steps, 200))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush.fill_(i & 255)
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        result[name] = sum(a.elapsed_time(b) for a, b in ev) / n
+    diff = (out_c.float() - out_p.float()).abs().max().item()
+    row = Hkv * D * 2 * 2
+    unique = (P + int(suffix.sum())) * row
+    logical = (S * P + int(suffix.sum())) * row
+    return dict(case=case, cascade_ms=result["cascade"], plain_ms=result["plain"], unique=unique, logical=logical,
+                max_diff=diff, launches=3 * n)
+
+
 def prefill_leg(args, dev, steps):
     import paged_kv_attention_gb300 as pa
     import workloads
@@ -480,13 +548,14 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "int8"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "int8", "cascade"], default="all",
                     help="run one leg only (profiling runs)")
     ap.add_argument("--decode-seqs", type=int, default=64, help="sequences of 4096 tokens in the decode leg")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the decode step eagerly, not as CUDA graphs")
     ap.add_argument("--no-int8", action="store_true", help="skip the int8-cache decode leg")
+    ap.add_argument("--no-cascade", action="store_true", help="skip the shared-prefix (cascade) decode leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -501,6 +570,14 @@ def main():
     peaks, peak_src = load_peaks()
     traffic = load_traffic()
 
+    if args.only == "cascade":
+        c = cascade_leg(args, dev)
+        if rank == 0:
+            print(json.dumps({"cascade_only": True, "cascade_us": round(c["cascade_ms"] * 1e3, 2),
+                              "plain_us": round(c["plain_ms"] * 1e3, 2),
+                              "saving": round(c["plain_ms"] / c["cascade_ms"], 3), "max_diff": c["max_diff"]}),
+                  flush=True)
+        return
     if args.only == "int8":
         q8 = decode_int8_leg(args, dev)
         if rank == 0:
@@ -511,6 +588,7 @@ def main():
         d = None if args.only == "prefill" else decode_leg(args, world, rank, dev)
         p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps)
         q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
+        cz = None if (args.no_cascade or args.only != "all") else cascade_leg(args, dev)
     clk = clocks.summary()
     if d is None:
         if rank == 0 and p is not None:
@@ -570,6 +648,17 @@ def main():
             "value": round(q8["gbs"], 2), "unit": "GB/s", "call_ms": round(q8["ms"], 5),
             "algorithmic_bytes_per_launch": q8["bytes"], "frac_of_hbm_peak": round(q8["gbs"] / hbm, 4),
             "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3), "traffic": traffic.get("decode_int8_kernel")}
+    if cz is not None:
+        cms = cz["cascade_ms"]
+        line["cascade"] = {
+            "workload": CASCADE_WORKLOAD + " (64 sequences, shared 4,000-token prefix, own suffixes of 1-256)",
+            "cascade_us": round(cms * 1e3, 2), "plain_decode_us": round(cz["plain_ms"] * 1e3, 2),
+            "saving": round(cz["plain_ms"] / cms, 3),
+            "logical_kv_bytes": cz["logical"], "unique_kv_bytes": cz["unique"],
+            "effective_GBps": round(cz["logical"] / (cms / 1e3) / 1e9, 1),
+            "unique_GBps": round(cz["unique"] / (cms / 1e3) / 1e9, 1),
+            "max_abs_diff_vs_plain": cz["max_diff"], "l2": "256 MB rewritten between timed calls",
+            "gpu_launches": cz["launches"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and case.num_reqs == 64:
         _, ko_vo = None, oracle_pools(case)
         v, dt, n, threads = time_oracle_decode(case, *ko_vo)

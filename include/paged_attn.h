@@ -245,6 +245,39 @@ pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const
 pa_status pa_selftest_wait_timeout(int limit_us, int32_t* error_word, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Cascade (shared-prefix) decode. "32. Production attention kernels", Long contexts: split the
+ * keys (the same merge serves cascade attention: attend to a shared prefix once for many
+ * requests, then merge with each request's own suffix) and Stretch exercises, item 2.
+ * Sequence s's context is the prefix_len positions of the shared prefix (pages
+ * prefix_table[0 .. cdiv(prefix_len, block_size))) followed by its own suffix_lens[s]
+ * positions (pages suffix_tables[s, ...]); its one query is the last of them, so
+ *   out[s, h] = softmax over prefix ++ suffix of (scale * q[s,h] . k) . v.
+ * The prefix's K/V is read once for all sequences: a tensor-core pass puts all S * (Hq/Hkv)
+ * query rows of a KV head against each key range of it (ranges sized to fill the SMs) and
+ * writes their unnormalised partials; the suffixes run as the split-KV decode; the combine
+ * merges all partials of a row by log-sum-exp. Three launches on `stream`; returns once they
+ * are enqueued. Errors: as pa_paged_attention_decode (PA_ERR_WORKSPACE_TOO_SMALL for a short
+ * workspace); a prefix_len outside [0, max_prefix_blocks * block_size] sets
+ * PA_ERRBIT_LENGTH_OUT_OF_RANGE and is clamped.
+ * --------------------------------------------------------------------------------------- */
+
+/* Workspace bytes that suffice for pa_cascade_decode with these sizes and any split count. */
+size_t pa_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int block_size,
+                                  int max_prefix_blocks, int max_blocks_per_seq);
+
+/*   q, out [S, Hq, D] bf16; k_cache, v_cache bf16 pools; prefix_table [max_prefix_blocks] int32;
+ *   prefix_len: DEVICE int32 scalar (so a captured graph follows a growing prefix); suffix_tables
+ *   [S, max_blocks_per_seq]; suffix_lens [S] (may be 0). num_splits: suffix splits (0 = auto, at most 31).
+ *   workspace: >= pa_cascade_workspace_bytes, 16-byte aligned, device memory; the caller owns it.
+ *   Supported: head_dim 128, Hq/Hkv in {1,2,4,8,16}, block_size in {16,32,64,128}. */
+pa_status pa_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* prefix_table, const int32_t* prefix_len, int max_prefix_blocks,
+                            const int32_t* suffix_tables, const int32_t* suffix_lens, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            int max_blocks_per_seq, float scale, int num_splits, void* out, void* workspace,
+                            size_t workspace_bytes, int32_t* error_word, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * 8-bit KV cache. "32. Production attention kernels", Quantized KV caches; "TileInfer.jl -
  * Attention kernels", INT8 cache. The pools hold one code per element ([num_blocks,
  * block_size, Hkv, D], int8 or fp8 E4M3) and one float32 scale per (slot, KV head)

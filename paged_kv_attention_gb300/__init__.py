@@ -18,6 +18,7 @@ from . import _lib
 
 __all__ = [
     "PagedAttentionError",
+    "cascade_decode",
     "decode_auto_splits",
     "decode_workspace_bytes",
     "plan_decode_splits",
@@ -163,6 +164,31 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
         _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
     _check("pa_paged_attention_varlen", st)
+    return out
+
+
+def cascade_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_table: torch.Tensor,
+                   prefix_len: torch.Tensor, suffix_tables: torch.Tensor, suffix_lens: torch.Tensor,
+                   scale: float | None = None, num_splits: int = 0, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, error_word: torch.Tensor | None = None,
+                   stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Decode of S sequences that share a cached prefix (``prefix_len``: a device int32 scalar)
+    followed by their own suffixes; the prefix K/V is read once for all of them."""
+    s, hq, d = q.shape
+    nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    mb = suffix_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.pa_cascade_workspace_bytes(s, hq, d, bs, prefix_table.numel(), mb)), 16),
+                                dtype=torch.uint8, device=q.device)
+    ws_len = workspace.numel() * workspace.element_size()
+    st = lib.pa_cascade_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_table), _ptr(prefix_len),
+                               prefix_table.numel(), _ptr(suffix_tables), _ptr(suffix_lens), s, hq, hkv, d, bs, nb,
+                               mb, float(scale or 0.0), int(num_splits), _ptr(out), _ptr(workspace), ws_len,
+                               _ptr(error_word), _stream(stream))
+    _check("pa_cascade_decode", st)
     return out
 
 

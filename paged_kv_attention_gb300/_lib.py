@@ -53,6 +53,9 @@ SIGNATURES = {
     "pa_paged_attention_decode_ex": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
                                           _p, _p, _sz, _opt, _p, _p]),
     "pa_selftest_wait_timeout": (_i, [_i, _p, _p]),
+    "pa_cascade_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "pa_cascade_decode": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p, _sz,
+                               _p, _p]),
     "pa_reshape_and_cache_quant": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _p, _p]),
     "pa_paged_attention_decode_quant": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f,
                                              _i, _p, _p, _sz, _opt, _p, _p]),

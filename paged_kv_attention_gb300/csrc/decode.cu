@@ -110,13 +110,13 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, const flo
       L += wt * ml[(w * rows + n) * 2 + 1];
       O += wt * mo[(w * rows + n) * D + d];
     }
-    if (p.num_splits == 1) {
+    if (p.num_splits == 1 && !p.force_partial) {
       if (p.sinks != nullptr) O *= fold_sink(p.sinks[h0 + n], M, L);
       const float v = (L > 0.f) ? O / L : 0.f;
       OutT* out = reinterpret_cast<OutT*>(p.out);
       out[((size_t)q_row * p.num_q_heads + h0 + n) * D + d] = static_cast<OutT>(v);
     } else {
-      const size_t slot = ((size_t)unit * p.num_splits + split) * p.num_q_heads + h0 + n;
+      const size_t slot = ((size_t)unit * p.slot_count + p.slot_offset + split) * p.num_q_heads + h0 + n;
       p.ws_acc[slot * D + d] = O;
       if (d == 0) {
         p.ws_ml[slot * 2] = M;
@@ -718,19 +718,27 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)unit * p.num_q_heads + h) * D;
   // every lane runs every iteration (the weight shuffles need the whole warp); lanes past
-  // the head dim only skip their loads and stores
+  // the head dim only skip their loads and stores. Eight partials' loads are issued before
+  // any of them is used, so their latencies overlap.
+  constexpr int kBatch = 8;
   for (int d0 = 0; d0 < D; d0 += 128) {
     const int d = d0 + lane * 4;
     const bool active = d < D;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      if (active) {
-        const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)s * p.num_q_heads) * D + d);
-        a.x = fmaf(ws, v.x, a.x);
-        a.y = fmaf(ws, v.y, a.y);
-        a.z = fmaf(ws, v.z, a.z);
-        a.w = fmaf(ws, v.w, a.w);
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        v[k] = (active && s0 + k < S)
+                   ? *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)(s0 + k) * p.num_q_heads) * D + d)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float ws = __shfl_sync(0xffffffffu, w, (s0 + k) & 31);  // w = 0 on lanes >= S
+        a.x = fmaf(ws, v[k].x, a.x);
+        a.y = fmaf(ws, v[k].y, a.y);
+        a.z = fmaf(ws, v[k].z, a.z);
+        a.w = fmaf(ws, v[k].w, a.w);
       }
     }
     if (active) {

@@ -237,6 +237,9 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   splits = (int)cdivll(max_chunks, per);
   p.num_splits = splits;
   p.chunks_per_split = per;
+  p.slot_count = splits;
+  p.slot_offset = 0;
+  p.force_partial = 0;
   if (splits > 1) {
     const size_t need = (size_t)p.num_units * splits * p.num_q_heads * ((size_t)D + 2) * 4;
     if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
@@ -585,4 +588,155 @@ extern "C" pa_status pa_selftest_wait_timeout(int limit_us, int32_t* error_word,
   return launch_wait_timeout_selftest((uint64_t)limit_us * 1000ull, error_word, as_stream(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------ cascade
+namespace {
+
+// The combine merges at most kMaxSplits partials per row: up to kMaxPrefixSplits key ranges
+// of the prefix, the rest for the suffix's splits.
+constexpr int kMaxPrefixSplits = 16;
+constexpr int kMinPrefixTilesPerSplit = 2;  // 256 keys: keeps the Q load and pipeline fill amortised
+
+struct CascadePlan {
+  int prefix_splits, prefix_per;  // key ranges of the prefix pass, 128-key tiles each
+  int suffix_splits, suffix_per;  // splits of the suffix decode, 16-key chunks each
+};
+
+long long prefix_tiles_bound(int max_prefix_blocks, int block_size) {
+  return cdivll((long long)max_prefix_blocks * block_size, 128);
+}
+
+// Prefix ranges fill the SMs for the q_tiles x Hkv tiles of the pass (the prefix length itself
+// is a device value: ranges past its end write neutral partials); the suffix gets the splits
+// the plain decode would pick, within what is left of the combine's budget.
+CascadePlan cascade_plan(DeviceInfo* info, int num_seqs, int Hkv, int D, int G, int block_size,
+                         int max_prefix_blocks, int max_blocks_per_seq, int num_splits) {
+  CascadePlan c;
+  const long long ptiles = prefix_tiles_bound(max_prefix_blocks, block_size);
+  const long long base_ctas = cdivll(num_seqs, varlen_tc_tokens_per_cta(G)) * Hkv;
+  long long ps = cdivll(info->sms, base_ctas);
+  ps = std::min<long long>(ps, std::min<long long>(kMaxPrefixSplits, cdivll(ptiles, kMinPrefixTilesPerSplit)));
+  ps = std::max<long long>(ps, 1);
+  c.prefix_per = (int)cdivll(ptiles, ps);
+  c.prefix_splits = (int)cdivll(ptiles, c.prefix_per);
+  const long long max_chunks = cdivll((long long)max_blocks_per_seq * block_size, kChunk);
+  int ss = num_splits > 0 ? num_splits : auto_splits(info, num_seqs, Hkv, D, G, max_chunks, PA_DTYPE_BF16);
+  ss = (int)std::min<long long>(std::min(ss, kMaxSplits - c.prefix_splits), max_chunks);
+  c.suffix_per = (int)cdivll(max_chunks, ss);
+  c.suffix_splits = (int)cdivll(max_chunks, c.suffix_per);
+  return c;
+}
+
+}  // namespace
+
+extern "C" size_t pa_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int block_size,
+                                             int max_prefix_blocks, int max_blocks_per_seq) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_prefix_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  const long long ptiles = prefix_tiles_bound(max_prefix_blocks, block_size);
+  const long long ps = std::min<long long>(kMaxPrefixSplits, cdivll(ptiles, kMinPrefixTilesPerSplit));
+  const long long max_chunks = cdivll((long long)max_blocks_per_seq * block_size, kChunk);
+  const long long slots = std::min<long long>(kMaxSplits, ps + max_chunks);
+  return (size_t)((long long)num_seqs * slots * num_q_heads * ((long long)head_dim + 2) * 4);
+}
+
+extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* prefix_table, const int32_t* prefix_len, int max_prefix_blocks,
+                                       const int32_t* suffix_tables, const int32_t* suffix_lens, int num_seqs,
+                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                       int num_blocks, int max_blocks_per_seq, float scale, int num_splits, void* out,
+                                       void* workspace, size_t workspace_bytes, int32_t* error_word, void* stream) {
+  if (num_seqs < 0 || num_splits < 0 || num_splits > kMaxSplits - 1 || max_prefix_blocks <= 0)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0) return PA_OK;
+  if (!prefix_table || !prefix_len || !suffix_lens) return PA_ERR_INVALID_ARGUMENT;
+  pa_status st = validate_common(q, k_cache, v_cache, suffix_tables, out, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, num_blocks, max_blocks_per_seq, scale, PA_DTYPE_BF16);
+  if (st != PA_OK) return st;
+  const int G = num_q_heads / num_kv_heads;
+  if (!varlen_tc_supported(head_dim, G, block_size)) return PA_ERR_UNSUPPORTED;
+  if ((long long)max_prefix_blocks * block_size > (1ll << 30)) return PA_ERR_UNSUPPORTED;
+  if ((long long)num_seqs * num_kv_heads * kMaxSplits > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
+  DeviceInfo* info = nullptr;
+  if (!device_info(&info)) return PA_ERR_CUDA;
+  cudaStream_t strm = as_stream(stream);
+  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+
+  const CascadePlan plan = cascade_plan(info, num_seqs, num_kv_heads, head_dim, G, block_size, max_prefix_blocks,
+                                        max_blocks_per_seq, num_splits);
+  const int slots = plan.prefix_splits + plan.suffix_splits;
+  const size_t need = (size_t)num_seqs * slots * num_q_heads * ((size_t)head_dim + 2) * 4;
+  if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return PA_ERR_INVALID_ARGUMENT;
+  float* ws_acc = static_cast<float*>(workspace);
+  float* ws_ml = ws_acc + (size_t)num_seqs * slots * num_q_heads * head_dim;
+
+  // 1. the shared prefix, read once per key range: all S * G query rows of a KV head against
+  //    its pages, partials to slots [0, prefix_splits)
+  VarlenParams vp{};
+  vp.block_tables = prefix_table;
+  vp.out = out;
+  vp.err = error_word;
+  vp.num_reqs = plan.prefix_splits;
+  vp.num_tokens = num_seqs;
+  vp.num_q_heads = num_q_heads;
+  vp.num_kv_heads = num_kv_heads;
+  vp.group = G;
+  vp.block_size = block_size;
+  vp.num_blocks = num_blocks;
+  vp.max_blocks = max_prefix_blocks;
+  vp.max_query_len = num_seqs;
+  vp.q_tiles = (int)cdivll(num_seqs, varlen_tc_tokens_per_cta(G));
+  vp.causal = 0;
+  vp.scale_log2 = sc * kLog2e;
+  vp.prefix_mode = 1;
+  vp.prefix_len = prefix_len;
+  vp.prefix_tiles_per_split = plan.prefix_per;
+  vp.ws_acc = ws_acc;
+  vp.ws_ml = ws_ml;
+  vp.slot_count = slots;
+  CUtensorMap qmap, kmap, vmap;
+  if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_seqs, G, 128 / G) ||
+      !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, block_size) ||
+      !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, block_size))
+    return PA_ERR_CUDA;
+  if (launch_varlen_tc(vp, qmap, kmap, vmap, strm) != cudaSuccess) return PA_ERR_CUDA;
+
+  // 2. each sequence's own suffix: the split-KV decode, partials to the slots after the prefix's
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = suffix_tables;
+  p.context_lens = suffix_lens;
+  p.out = out;
+  p.err = error_word;
+  p.num_units = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = G;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.scale_log2 = sc * kLog2e;
+  p.num_splits = plan.suffix_splits;
+  p.chunks_per_split = plan.suffix_per;
+  p.ws_acc = ws_acc;
+  p.ws_ml = ws_ml;
+  p.force_partial = 1;
+  p.slot_offset = plan.prefix_splits;
+  p.slot_count = slots;
+  CUtensorMap skmap, svmap;
+  if (!encode_cache_map(&skmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk) ||
+      !encode_cache_map(&svmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk))
+    return PA_ERR_CUDA;
+  if (launch_decode_bf16(p, skmap, svmap, strm) != cudaSuccess) return PA_ERR_CUDA;
+
+  // 3. merge every row's prefix and suffix partials (the split-KV combine over all its slots)
+  DecodeParams c = p;
+  c.num_splits = slots;
+  return launch_combine(c, PA_DTYPE_BF16, strm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

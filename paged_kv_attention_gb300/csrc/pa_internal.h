@@ -51,6 +51,11 @@ struct DecodeParams {
   int quant;
   const float* k_scales;
   const float* v_scales;
+  // partial-slot addressing: split `s` of unit `u` is slot u * slot_count + slot_offset + s;
+  // force_partial writes partials even with one split (the cascade's suffix pass)
+  int force_partial;
+  int slot_offset;
+  int slot_count;
 };
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
@@ -99,6 +104,16 @@ struct VarlenParams {
   float softcap_log2;
   float scale_over_cap;
   const float* sinks;
+  // cascade prefix pass: all num_tokens query rows, non-causal over the prefix pages
+  // (block_tables row 0) of length *prefix_len, cut into num_reqs key ranges of
+  // prefix_tiles_per_split 128-key tiles; range r of row t writes its unnormalised partial to
+  // slot t * slot_count + r of ws_acc / ws_ml instead of `out`
+  int prefix_mode;
+  const int32_t* prefix_len;
+  int prefix_tiles_per_split;
+  float* ws_acc;
+  float* ws_ml;
+  int slot_count;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
 int varlen_tc_tokens_per_cta(int group);

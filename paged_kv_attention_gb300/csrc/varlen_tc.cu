@@ -215,6 +215,9 @@ __device__ __forceinline__ TileSpan tile_span(int tok0, int TOK, int q_len, int 
   return t;
 }
 
+// kPrefix: the cascade's shared-prefix pass (one request of num_tokens query rows that all
+// see the whole prefix; unnormalised partials out instead of normalised rows).
+template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_tc_kernel(const __grid_constant__ VarlenParams p, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
@@ -229,19 +232,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int per_tile = p.num_reqs * p.num_kv_heads;
   const int tile = p.q_tiles - 1 - (int)(blockIdx.x / per_tile);
   const int rem = (int)(blockIdx.x % per_tile);
-  const int r = rem / p.num_kv_heads;
+  const int r = rem / p.num_kv_heads;  // the request, or the prefix key range in prefix mode
   const int kvh = rem - r * p.num_kv_heads;
   const int G = p.group;
   const int TOK = kBM / G;  // tokens per 128-row tile; a CTA covers 2 * TOK tokens
   const int tid = threadIdx.x;
 
-  const int q_start = p.query_start_loc[r];
-  const int q_stop = p.query_start_loc[r + 1];
-  const int seq_len = p.seq_lens[r];
+  int q_start, q_stop, seq_len;
+  if (kPrefix) {
+    // the cascade's shared prefix: every query row attends to all of it
+    q_start = 0;
+    q_stop = p.num_tokens;
+    seq_len = *p.prefix_len;
+    const int cap = p.max_blocks * p.block_size;
+    if (seq_len < 0 || seq_len > cap) {
+      if (tid == 0 && kvh == 0 && tile == 0) flag_error(p.err, PA_ERRBIT_LENGTH_OUT_OF_RANGE);
+      seq_len = seq_len < 0 ? 0 : cap;
+    }
+  } else {
+    q_start = p.query_start_loc[r];
+    q_stop = p.query_start_loc[r + 1];
+    seq_len = p.seq_lens[r];
+  }
   const int q_len = q_stop - q_start;
   const bool layout_ok = q_start >= 0 && q_len >= 0 && q_stop <= p.num_tokens;
   const bool too_long = seq_len > p.max_blocks * p.block_size;
-  const bool bad = !layout_ok || q_len > seq_len || too_long;
+  const bool bad = !layout_ok || (!kPrefix && (q_len > seq_len || too_long));
   const int tok0 = tile * 2 * TOK;
   if (bad) {
     if (tid == 0 && kvh == 0 && tile == 0)
@@ -265,13 +281,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const TileSpan spanB = tile_span(tok0 + TOK, TOK, q_len, seq_len, p.causal);
   // Iteration i covers key tile j0 + i. Under a sliding window, j0 is the tile holding the
   // oldest key the CTA's first query sees; tiles before it are never loaded.
-  const int j0 = p.window > 0 ? max(0, spanA.first - p.window + 1) / kBN : 0;
-  const int nA = spanA.n_kv - j0;
-  const int nB = spanB.n_kv > 0 ? spanB.n_kv - j0 : 0;
+  // In prefix mode the CTA covers key tiles [j0, j0 + prefix_tiles_per_split) of the prefix.
+  const int j0 = kPrefix          ? r * p.prefix_tiles_per_split
+                 : p.window > 0 ? max(0, spanA.first - p.window + 1) / kBN
+                                : 0;
+  const int endA = kPrefix ? min(spanA.n_kv, j0 + p.prefix_tiles_per_split) : spanA.n_kv;
+  const int endB = kPrefix ? min(spanB.n_kv, j0 + p.prefix_tiles_per_split) : spanB.n_kv;
+  const int nA = max(0, endA - j0);
+  const int nB = spanB.n_kv > 0 ? max(0, endB - j0) : 0;
   const int n_kv = max(nA, nB);
   const int bs = p.block_size;
   const int pages_per_tile = kBN / bs;
   const int seq_pages = (seq_len + bs - 1) / bs;
+  if (kPrefix && n_kv <= 0) {
+    // no prefix keys in this range (a short or empty prefix): the neutral partial (0, -inf, 0)
+    const int rows = min(2 * TOK, q_len - tok0) * G;
+    for (int i = tid; i < rows * (kD / 4); i += blockDim.x) {
+      const int row = i / (kD / 4), c = i % (kD / 4);
+      const size_t slot = ((size_t)(q_start + tok0 + row / G) * p.slot_count + r) * p.num_q_heads + kvh * G + row % G;
+      *reinterpret_cast<float4*>(p.ws_acc + slot * kD + c * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c == 0) {
+        p.ws_ml[slot * 2] = -INFINITY;
+        p.ws_ml[slot * 2 + 1] = 0.f;
+      }
+    }
+    return;
+  }
 
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -304,7 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
-    // ------------------------------------------------ producer: Q_A, Q_B once, then K/V tiles
+    // ------------------------------------------------ producer: Q_A, Q_B once, then K/V tiles.
+    // The whole warp walks the loop: page ids arrive 32 at a time (one coalesced load, one per
+    // lane, a tile never straddles two 32-page windows since its page count divides 32) and
+    // are handed out by shuffle; lane 0 issues the copies.
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
@@ -314,39 +352,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a)
           tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
                       q_start + tok0 + t * TOK);
-      const int32_t* table = p.block_tables + (size_t)r * p.max_blocks;
-      for (int i = 0; i < n_kv; ++i) {
-        const int st = i % kStages;
-        const uint32_t round_parity = ((i / kStages) - 1) & 1;
-        const int p0 = (j0 + i) * pages_per_tile;
-        const int p1 = min(p0 + pages_per_tile, seq_pages);
-        const uint32_t bytes = (uint32_t)(p1 - p0) * bs * 256u;
-        if (i >= kStages && !wait_or_abort(&bars[B_KE + st], round_parity, abort_flag)) {
-          set_abort(abort_flag, p.err);
-          break;
-        }
+    }
+    const int32_t* table = p.block_tables + (size_t)(kPrefix ? 0 : r) * p.max_blocks;
+    int win_base = -32, my_page = -1;
+    for (int i = 0; i < n_kv; ++i) {
+      const int st = i % kStages;
+      const uint32_t round_parity = ((i / kStages) - 1) & 1;
+      const int p0 = (j0 + i) * pages_per_tile;
+      const int np = min(p0 + pages_per_tile, seq_pages) - p0;
+      const uint32_t bytes = (uint32_t)np * bs * 256u;
+      if ((p0 & ~31) != win_base) {
+        win_base = p0 & ~31;
+        my_page = win_base + lane < p.max_blocks ? __ldg(table + win_base + lane) : -1;
+      }
+      int pages[8];  // pages_per_tile <= 8 (block size >= 16)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pages[k] = __shfl_sync(0xffffffffu, my_page, (p0 - win_base + k) & 31);
+      if (i >= kStages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
+        if (lane == 0) set_abort(abort_flag, p.err);
+        break;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars[B_KF + st], bytes);
-        for (int pg = p0; pg < p1; ++pg) {
-          const int page = table[pg];
-          if (page < 0 || page >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k >= np) break;
+          if (pages[k] < 0 || pages[k] >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // zeros
           for (int a = 0; a < 2; ++a)
-            tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + (pg - p0) * bs * 128, &kmap,
-                        &bars[B_KF + st], a * 64, kvh, 0, page);
+            tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + k * bs * 128, &kmap, &bars[B_KF + st],
+                        a * 64, kvh, 0, pages[k]);
         }
-        if (i >= kStages && !wait_or_abort(&bars[B_VE + st], round_parity, abort_flag)) {
+      }
+      if (i >= kStages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
+        if (lane == 0) {
           set_abort(abort_flag, p.err);
           *issued_tiles = i + 1;  // K of iteration i is in flight
-          break;
         }
+        break;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
-        for (int pg = p0; pg < p1; ++pg) {
-          const int page = table[pg];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k >= np) break;
           for (int a = 0; a < 2; ++a)
-            tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + (pg - p0) * bs * 128, &vmap,
-                        &bars[B_VF + st], a * 64, kvh, 0, page);
+            tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + k * bs * 128, &vmap, &bars[B_VF + st],
+                        a * 64, kvh, 0, pages[k]);
         }
         *issued_tiles = i + 1;
       }
+      __syncwarp();
     }
   } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer (lane 0); the warp zeroes V tails
@@ -547,28 +602,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[B_PR + t]);
     }
     if (ok && n_mine > 0 && !warp_wait(&bars[B_OD + t], (n_mine - 1) & 1, abort_flag)) ok = false;
+    // Epilogue. Each warp stages its 32 rows in the tile's Q buffer (free by now: every MMA
+    // that read it completed before the last P.V) and writes them out two rows per store
+    // instruction, 256 contiguous bytes per row, instead of 32 rows' scattered 16-byte pieces.
+    // Staged 16-byte chunks are XOR-swizzled by row so neither side conflicts on banks.
+    uint8_t* stage = smem + kOffQ + t * kTileBytes + (warp & 3) * (32 * 256);
+    auto put = [&](int c, uint4 v) { *reinterpret_cast<uint4*>(stage + lane * 256 + ((c ^ (lane & 15)) << 4)) = v; };
+    // row rr of this warp's 32: its position in the batch, or -1 past the request's queries
+    auto row_token = [&](int rr) {
+      const int R = (warp & 3) * 32 + rr;
+      const int tk = tok0 + t * TOK + R / G;
+      return tk < q_len ? q_start + tk : -1;
+    };
+    const int head0 = kvh * G;
     if (!ok) {
       set_abort(abort_flag, p.err);
+    } else if (kPrefix) {
+      // cascade prefix pass: the row's unnormalised partial (acc, m in log2 units, l) in the
+      // split-partial layout the combine merges. (A tile without keys here has no valid rows:
+      // ranges past the prefix end left the kernel at the top.)
+      if (n_mine > 0) {
+        tc_fence_after();
+        if (row_valid) {
+          const size_t slot = ((size_t)(q_start + tok) * p.slot_count + r) * p.num_q_heads + head0 + row % G;
+          p.ws_ml[slot * 2] = m_run;
+          p.ws_ml[slot * 2 + 1] = l_run;
+        }
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {  // 64 accumulator columns (256 bytes of fp32) per pass
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t ov[32];
+            tmem_ld32(o_col + 64 * h + 32 * q2, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              put(q2 * 8 + i, make_uint4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]));
+          }
+          __syncwarp();
+#pragma unroll 4
+          for (int k = 0; k < 16; ++k) {
+            const int rr = 2 * k + (lane >> 4);
+            const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + (((lane & 15) ^ (rr & 15)) << 4));
+            const int tk = row_token(rr);
+            if (tk >= 0) {
+              const int R = (warp & 3) * 32 + rr;
+              const size_t slot = ((size_t)tk * p.slot_count + r) * p.num_q_heads + head0 + R % G;
+              *reinterpret_cast<uint4*>(p.ws_acc + slot * kD + 64 * h + (lane & 15) * 4) = v;
+            }
+          }
+          __syncwarp();
+        }
+      }
     } else if (n_mine > 0) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                           ((size_t)(q_start + tok) * p.num_q_heads + kvh * G + row % G) * kD;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t ov[32];
         tmem_ld32(o_col + 32 * q4, ov);
         tmem_ld_wait();
-        if (row_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
-            *reinterpret_cast<uint4*>(out + q4 * 32 + i) = w;
-          }
+        for (int i = 0; i < 32; i += 8) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+          put(q4 * 4 + i / 8, w);
+        }
+      }
+      __syncwarp();
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int rr = 2 * k + (lane >> 4);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + (((lane & 15) ^ (rr & 15)) << 4));
+        const int tk = row_token(rr);
+        if (tk >= 0) {
+          const int R = (warp & 3) * 32 + rr;
+          *reinterpret_cast<uint4*>(out + ((size_t)tk * p.num_q_heads + head0 + R % G) * kD + (lane & 15) * 8) = v;
         }
       }
     }
@@ -610,18 +723,20 @@ int varlen_tc_tokens_per_cta(int group) { return 2 * (kBM / group); }
 
 cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+  static bool attr_done[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(varlen_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const int mode = p.prefix_mode ? 1 : 0;
+  auto kern = p.prefix_mode ? varlen_tc_kernel<true> : varlen_tc_kernel<false>;
+  if (dev < 64 && !attr_done[dev][mode]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev][mode] = true;
   }
   const long long ctas = (long long)p.q_tiles * p.num_reqs * p.num_kv_heads;
   if (ctas <= 0) return cudaSuccess;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  varlen_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(p, qmap, kmap, vmap);
+  kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(p, qmap, kmap, vmap);
   return cudaGetLastError();
 }
 

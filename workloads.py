@@ -199,6 +199,22 @@ def prefill_4x8192_bf16() -> PagedCase:
                      num_kv_heads=8, head_dim=128, block_size=64, dtype=torch.bfloat16)
 
 
+def cascade_case(name: str, seed: int, prefix_len: int, suffix_lens: list[int], **kw) -> PagedCase:
+    """S decode sequences behind one shared cached prefix: request 0 holds the prefix's
+    prefix_len positions (no query), request 1 + s the s-th sequence's own suffix_lens[s]
+    positions and its one query. The prefix's pages are block_tables[0]."""
+    return make_case(name, seed, [0] + [1] * len(suffix_lens), [prefix_len] + list(suffix_lens), **kw)
+
+
+def cascade_64x4000_bf16() -> PagedCase:
+    """64 sequences sharing a 4,000-token prefix (250 pages of 16), each with its own suffix of
+    1..256 positions (uniform); 32 q / 8 KV heads, head_dim 128, bf16."""
+    gen = torch.Generator().manual_seed(1006)
+    suffix = torch.randint(1, 257, (64,), generator=gen).tolist()
+    return cascade_case("cascade_64x4000_bf16", 1006, 4000, suffix, num_q_heads=32, num_kv_heads=8,
+                        head_dim=128, block_size=16, dtype=torch.bfloat16, gen=gen)
+
+
 NAMED = {
     "decode_1seq_fp32": decode_1seq_fp32,
     "decode_ragged32_bf16": decode_ragged32_bf16,
@@ -206,4 +222,5 @@ NAMED = {
     "decode_64x4096_bf16_d256": lambda: decode_64x4096_bf16(256),
     "varlen_mixed_bf16": varlen_mixed_bf16,
     "prefill_4x8192_bf16": prefill_4x8192_bf16,
+    "cascade_64x4000_bf16": cascade_64x4000_bf16,
 }
