@@ -283,6 +283,20 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Decode (one query per sequence): the block-table row is the unit, and this split's first
+  // page is known before its length is, so the producer starts its first page-id window load
+  // now and the two memory latencies overlap. (A window that turns out to start later than
+  // the split is simply reloaded.)
+  int spec_base = -64, spec_page = -1;
+  if (warp == C::kConsumers && lane == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (!p.varlen && warp == C::kConsumers) {
+    spec_base = split * p.chunks_per_split * kChunk / p.block_size;
+    spec_page = spec_base + lane < p.max_blocks ? __ldg(p.block_tables + (size_t)unit * p.max_blocks + spec_base + lane)
+                                                : -1;
+  }
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
   const int n_chunks = (u.len + kChunk - 1) / kChunk;
   const int c_begin = max(split * p.chunks_per_split, u.start / kChunk);
@@ -304,14 +318,10 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   if (warp == C::kConsumers) {
     // ---------------- producer: page-table walk + TMA (and, for 8-bit caches, the scales)
     if (n_mine > 0) {
-      if (lane == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-      }
       const int32_t* table = p.block_tables + (size_t)u.table_row * p.max_blocks;
       // page ids are fetched 32 at a time, one per lane, and handed out by shuffle: one
       // table-load latency per 32 pages instead of one per chunk
-      int win_base = -64, my_page = -1;
+      int win_base = spec_base, my_page = spec_page;
       int issued = 0;
       for (int i = 0; i < n_mine; ++i) {
         const int stage = i % C::kStages;
@@ -550,6 +560,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     }
   }
   __syncthreads();
+  // every CTA of the grid past its key loop lets a combine launched with programmatic stream
+  // serialisation start its launch (it waits for this grid's completion before reading)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (s_timeout && threadIdx.x == C::kConsumers * 32) {
     // wind down: let copies still in flight land before the CTA's shared memory is released
     const int issued = s_issued;
@@ -696,6 +709,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= p.num_units * p.num_q_heads) return;
+  // launched as a programmatic dependent of the split kernel: wait for that grid to complete
+  // and its partials to be visible (a no-op for an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int unit = gw / p.num_q_heads;
   const int h = gw - unit * p.num_q_heads;
   const int S = p.num_splits;
@@ -718,9 +734,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)unit * p.num_q_heads + h) * D;
   // every lane runs every iteration (the weight shuffles need the whole warp); lanes past
-  // the head dim only skip their loads and stores. Eight partials' loads are issued before
+  // the head dim only skip their loads and stores. Sixteen partials' loads are issued before
   // any of them is used, so their latencies overlap.
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;
   for (int d0 = 0; d0 < D; d0 += 128) {
     const int d = d0 + lane * 4;
     const bool active = d < D;
@@ -886,11 +902,20 @@ int decode_f32_ctas_per_sm(int head_dim, int group) {
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
   const long long warps = (long long)p.num_units * p.num_q_heads;
   const unsigned blocks = (unsigned)((warps + 3) / 4);
-  if (dtype == PA_DTYPE_BF16)
-    combine_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(p);
-  else
-    combine_kernel<float><<<blocks, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the combine's CTAs launch while the split kernel's last CTAs
+  // merge and store, and wait in-kernel for its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dtype == PA_DTYPE_BF16) return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
 }
 
 }  // namespace pa

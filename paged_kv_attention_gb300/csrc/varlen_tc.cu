@@ -339,10 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
-    // ------------------------------------------------ producer: Q_A, Q_B once, then K/V tiles.
-    // The whole warp walks the loop: page ids arrive 32 at a time (one coalesced load, one per
-    // lane, a tile never straddles two 32-page windows since its page count divides 32) and
-    // are handed out by shuffle; lane 0 issues the copies.
+    // ------------------------------------------------ producer (lane 0): Q_A, Q_B once, then K/V
+    // tiles. The page ids of tile i+1 are loaded while tile i's copies are issued and its
+    // stages wait to be freed, so no table load sits between two copies.
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
@@ -352,56 +351,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a)
           tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
                       q_start + tok0 + t * TOK);
-    }
-    const int32_t* table = p.block_tables + (size_t)(kPrefix ? 0 : r) * p.max_blocks;
-    int win_base = -32, my_page = -1;
-    for (int i = 0; i < n_kv; ++i) {
-      const int st = i % kStages;
-      const uint32_t round_parity = ((i / kStages) - 1) & 1;
-      const int p0 = (j0 + i) * pages_per_tile;
-      const int np = min(p0 + pages_per_tile, seq_pages) - p0;
-      const uint32_t bytes = (uint32_t)np * bs * 256u;
-      if ((p0 & ~31) != win_base) {
-        win_base = p0 & ~31;
-        my_page = win_base + lane < p.max_blocks ? __ldg(table + win_base + lane) : -1;
-      }
-      int pages[8];  // pages_per_tile <= 8 (block size >= 16)
+      const int32_t* table = p.block_tables + (size_t)(kPrefix ? 0 : r) * p.max_blocks;
+      // ids of tile i's pages (pages_per_tile <= 8 since the block size is >= 16)
+      auto load_ids = [&](int i, int (&ids)[8]) {
+        const int p0 = (j0 + i) * pages_per_tile;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) pages[k] = __shfl_sync(0xffffffffu, my_page, (p0 - win_base + k) & 31);
-      if (i >= kStages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
-        if (lane == 0) set_abort(abort_flag, p.err);
-        break;
-      }
-      if (lane == 0) {
+        for (int k = 0; k < 8; ++k) ids[k] = (k < pages_per_tile && p0 + k < seq_pages) ? __ldg(table + p0 + k) : 0;
+      };
+      int cur[8], nxt[8];
+      load_ids(0, cur);
+      for (int i = 0; i < n_kv; ++i) {
+        const int st = i % kStages;
+        const uint32_t round_parity = ((i / kStages) - 1) & 1;
+        const int p0 = (j0 + i) * pages_per_tile;
+        const int np = min(p0 + pages_per_tile, seq_pages) - p0;
+        const uint32_t bytes = (uint32_t)np * bs * 256u;
+        if (i + 1 < n_kv) load_ids(i + 1, nxt);
+        if (i >= kStages && !wait_or_abort(&bars[B_KE + st], round_parity, abort_flag)) {
+          set_abort(abort_flag, p.err);
+          break;
+        }
         mbar_arrive_expect_tx(&bars[B_KF + st], bytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           if (k >= np) break;
-          if (pages[k] < 0 || pages[k] >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // zeros
+          if (cur[k] < 0 || cur[k] >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
           for (int a = 0; a < 2; ++a)
             tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + k * bs * 128, &kmap, &bars[B_KF + st],
-                        a * 64, kvh, 0, pages[k]);
+                        a * 64, kvh, 0, cur[k]);
         }
-      }
-      if (i >= kStages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
-        if (lane == 0) {
+        if (i >= kStages && !wait_or_abort(&bars[B_VE + st], round_parity, abort_flag)) {
           set_abort(abort_flag, p.err);
           *issued_tiles = i + 1;  // K of iteration i is in flight
+          break;
         }
-        break;
-      }
-      if (lane == 0) {
         mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           if (k >= np) break;
           for (int a = 0; a < 2; ++a)
             tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + k * bs * 128, &vmap, &bars[B_VF + st],
-                        a * 64, kvh, 0, pages[k]);
+                        a * 64, kvh, 0, cur[k]);
         }
         *issued_tiles = i + 1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) cur[k] = nxt[k];
       }
-      __syncwarp();
     }
   } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer (lane 0); the warp zeroes V tails
@@ -602,86 +597,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[B_PR + t]);
     }
     if (ok && n_mine > 0 && !warp_wait(&bars[B_OD + t], (n_mine - 1) & 1, abort_flag)) ok = false;
-    // Epilogue. Each warp stages its 32 rows in the tile's Q buffer (free by now: every MMA
-    // that read it completed before the last P.V) and writes them out two rows per store
-    // instruction, 256 contiguous bytes per row, instead of 32 rows' scattered 16-byte pieces.
-    // Staged 16-byte chunks are XOR-swizzled by row so neither side conflicts on banks.
-    uint8_t* stage = smem + kOffQ + t * kTileBytes + (warp & 3) * (32 * 256);
-    auto put = [&](int c, uint4 v) { *reinterpret_cast<uint4*>(stage + lane * 256 + ((c ^ (lane & 15)) << 4)) = v; };
-    // row rr of this warp's 32: its position in the batch, or -1 past the request's queries
-    auto row_token = [&](int rr) {
-      const int R = (warp & 3) * 32 + rr;
-      const int tk = tok0 + t * TOK + R / G;
-      return tk < q_len ? q_start + tk : -1;
-    };
-    const int head0 = kvh * G;
     if (!ok) {
       set_abort(abort_flag, p.err);
     } else if (kPrefix) {
       // cascade prefix pass: the row's unnormalised partial (acc, m in log2 units, l) in the
       // split-partial layout the combine merges. (A tile without keys here has no valid rows:
       // ranges past the prefix end left the kernel at the top.)
+      const size_t slot = ((size_t)(q_start + tok) * p.slot_count + r) * p.num_q_heads + kvh * G + row % G;
+      float* acc = p.ws_acc + slot * kD;
       if (n_mine > 0) {
         tc_fence_after();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t ov[32];
+          tmem_ld32(o_col + 32 * q4, ov);
+          tmem_ld_wait();
+          if (row_valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<uint4*>(acc + q4 * 32 + i) = make_uint4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+          }
+        }
         if (row_valid) {
-          const size_t slot = ((size_t)(q_start + tok) * p.slot_count + r) * p.num_q_heads + head0 + row % G;
           p.ws_ml[slot * 2] = m_run;
           p.ws_ml[slot * 2 + 1] = l_run;
-        }
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {  // 64 accumulator columns (256 bytes of fp32) per pass
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            uint32_t ov[32];
-            tmem_ld32(o_col + 64 * h + 32 * q2, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              put(q2 * 8 + i, make_uint4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]));
-          }
-          __syncwarp();
-#pragma unroll 4
-          for (int k = 0; k < 16; ++k) {
-            const int rr = 2 * k + (lane >> 4);
-            const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + (((lane & 15) ^ (rr & 15)) << 4));
-            const int tk = row_token(rr);
-            if (tk >= 0) {
-              const int R = (warp & 3) * 32 + rr;
-              const size_t slot = ((size_t)tk * p.slot_count + r) * p.num_q_heads + head0 + R % G;
-              *reinterpret_cast<uint4*>(p.ws_acc + slot * kD + 64 * h + (lane & 15) * 4) = v;
-            }
-          }
-          __syncwarp();
         }
       }
     } else if (n_mine > 0) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                           ((size_t)(q_start + tok) * p.num_q_heads + kvh * G + row % G) * kD;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t ov[32];
         tmem_ld32(o_col + 32 * q4, ov);
         tmem_ld_wait();
+        if (row_valid) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
-          put(q4 * 4 + i / 8, w);
-        }
-      }
-      __syncwarp();
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 4
-      for (int k = 0; k < 16; ++k) {
-        const int rr = 2 * k + (lane >> 4);
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + (((lane & 15) ^ (rr & 15)) << 4));
-        const int tk = row_token(rr);
-        if (tk >= 0) {
-          const int R = (warp & 3) * 32 + rr;
-          *reinterpret_cast<uint4*>(out + ((size_t)tk * p.num_q_heads + head0 + R % G) * kD + (lane & 15) * 8) = v;
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+            *reinterpret_cast<uint4*>(out + q4 * 32 + i) = w;
+          }
         }
       }
     }
