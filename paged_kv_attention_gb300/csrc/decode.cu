@@ -26,6 +26,16 @@
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
+// Producer warps per decode CTA (measured at 64x4096 on GB300: one producer warp cannot issue
+// the page walk's copies as fast as HBM delivers them; 2 for bf16 took the call from 187 to 171 us,
+// 4 for 8-bit codes from 194 to 161 us; more warps cost occupancy)
+#ifndef PA_DECODE_PRODUCERS_BF16
+#define PA_DECODE_PRODUCERS_BF16 2
+#endif
+#ifndef PA_DECODE_PRODUCERS_CODES
+#define PA_DECODE_PRODUCERS_CODES 4
+#endif
+
 namespace pa {
 namespace {
 
@@ -163,70 +173,70 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // QK selects the cache format: 0 = bf16 values; 1 = int8 codes, 2 = fp8 E4M3 codes, each with
-// one fp32 scale per (slot, KV head). 8-bit codes are converted exactly to 16-bit values in
-// shared memory; the key's scale multiplies its scores and the value's scale its probabilities
-// before P.V ("TileInfer.jl - Attention kernels", INT8 cache). The page converts to bf16; here
-// the 16-bit type is fp16, which holds every code exactly and converts from int8 in about one
-// instruction per code (from bf16 it would take three), so the MMAs for 8-bit caches run in fp16
-// with fp32 accumulation, the queries converted once per CTA (exact within fp16's range) and the
-// probabilities rounded to fp16 (3 more mantissa bits than bf16).
+// one fp32 scale per (slot, KV head). 8-bit codes go from the ring straight into MMA operand
+// registers (ldmatrix over byte pairs) and are converted there, exactly, to fp16; the key's scale
+// multiplies its scores and the value's scale its probabilities before P.V ("TileInfer.jl -
+// Attention kernels", INT8 cache). The page converts to bf16; here the 16-bit type is fp16, which
+// holds every code exactly and converts from int8 in two instructions per two codes (from bf16 it
+// would take three), so the MMAs for 8-bit caches run in fp16 with fp32 accumulation, the queries
+// converted once per CTA (exact within fp16's range) and the probabilities rounded to fp16 (3
+// more mantissa bits than bf16).
+//
+// Register-direct operands rest on two permutations the products do not see. Scores: an
+// ldmatrix of byte pairs hands a thread 4 consecutive codes of a key row, so the k-slots
+// (2t, 2t+1 | 2t+8, 2t+9) of the m16n8k16 A fragment hold head dims (4t, 4t+1 | 4t+2, 4t+3) of
+// each 16-dim step, and the queries are loaded with the same order (a dot product is invariant
+// under a common permutation of its terms). P.V: a transposing ldmatrix hands a thread keys
+// (2t, 2t+1) of the dim pair (2g, 2g+1), so A rows g and g+8 of each 16-dim block are head dims
+// 2g and 2g+1; the accumulator rows are written back to those dims.
 template <int D, int QK>
 struct DecCfg {
   static constexpr int kConsumers = 4;
-  static constexpr int kThreads = (kConsumers + 1) * 32;
+  // producer warps take the chunks in turn
+  static constexpr int kProducers = QK ? PA_DECODE_PRODUCERS_CODES : PA_DECODE_PRODUCERS_BF16;
+  static constexpr int kThreads = (kConsumers + kProducers) * 32;
   static constexpr int kElt = QK ? 1 : 2;                // bytes per cached element
   static constexpr int kBoxes = D * kElt / 128;          // 128-byte swizzle columns of a cached row
-  static constexpr int kDChunks = D / 64;                // 128-byte columns of a bf16 row
   static constexpr int kTileBytes = kChunk * D * kElt;   // K or V rows of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = (QK ? 32768 : 65536) / kStageBytes;  // 64 KiB ring (32 KiB for codes)
+  // a 64 KiB ring: 8 stages of 8 KiB for bf16 at D 128; 16 stages of 4 KiB for codes at D 128
+  static constexpr int kStages = 65536 / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMT = D / 16;
-  // bf16 staging of converted codes: per consumer a K and a V tile of kDChunks column halves,
-  // each half 16 bytes further than a plain 2 KiB step so the conversion's stores to the two
-  // halves of one row fall on different banks (the swizzle is applied per row, so reads are
-  // unaffected)
-  static constexpr int kStageRegion = kChunk * 128 + 16;
-  static constexpr int kStagingTile = ((D / 64) * kStageRegion + 127) / 128 * 128;
-  static constexpr int kStagingBytes = QK ? kConsumers * 2 * kStagingTile : 0;
   static constexpr int kScaleBytes = QK ? kStages * 32 * 4 : 0;                   // 16 K + 16 V scales per stage
-  // ring | staging | full, empty barriers | merge (m, l) | scales; the merge accumulators alias the ring
-  static constexpr int kSmemBytes =
-      1024 + kRingBytes + kStagingBytes + 2 * kStages * 8 + kConsumers * 16 * 2 * 4 + kScaleBytes;
+  // ring | full, empty barriers | merge (m, l) | scales; the merge accumulators alias the ring
+  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kConsumers * 16 * 2 * 4 + kScaleBytes;
   static_assert(kBoxes >= 1, "a cached row must span at least one 128-byte column");
   static_assert(kStages % kConsumers == 0, "stages are dealt to consumers round robin");
-  static_assert(kConsumers * 16 * D * 4 <= kRingBytes + kStagingBytes, "merge area must fit in ring + staging");
+  // each stage must always be refilled by the same producer warp, so that it waits on the
+  // stage's "empty" phases in order: a parity wait cannot tell phase j from phase j - 2, and a
+  // producer running a ring lap ahead of another would take a stage still in use
+  static_assert(kStages % kProducers == 0, "stages are dealt to producers round robin");
+  static_assert(kConsumers * 16 * D * 4 <= kRingBytes, "merge area must fit in the ring");
 };
 
-// 16 codes (one 16-byte unit) -> 16 fp16 (two 16-byte units), exactly (|int8 code| <= 128 and
-// every E4M3 value are fp16 values).
+// Two codes of a 4-code word (bytes `sel` picks: byte 0 and byte 1 of the selector's low nibbles)
+// -> an fp16 pair, exactly (|int8 code| <= 128 and every E4M3 value are fp16 values).
+// int8: code c -> byte c + 128 -> the fp16 with bits 0x64bb is 1024 + b, so subtracting 1152
+// leaves c: one byte permute and one packed subtraction per two codes.
 template <int QK>
-__device__ __forceinline__ void codes_to_f16(uint4 raw, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (QK == 1) {
-      // code c -> byte b = c + 128; the fp16 with bits 0x64bb is 1024 + b, so subtracting
-      // 1152 gives c exactly: two byte permutes and two packed subtractions per four codes
-      const uint32_t y = w[k] ^ 0x80808080u;
-      const uint32_t h01 = __byte_perm(y, 0x64646464u, 0x5140);
-      const uint32_t h23 = __byte_perm(y, 0x64646464u, 0x5342);
-      const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
-      const __half2 c01 = __hsub2(*reinterpret_cast<const __half2*>(&h01), bias);
-      const __half2 c23 = __hsub2(*reinterpret_cast<const __half2*>(&h23), bias);
-      o[2 * k] = *reinterpret_cast<const uint32_t*>(&c01);
-      o[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&c23);
-    } else {
-      const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] & 0xffffu), __NV_E4M3);
-      const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] >> 16), __NV_E4M3);
-      o[2 * k] = (uint32_t)h01.x | ((uint32_t)h01.y << 16);
-      o[2 * k + 1] = (uint32_t)h23.x | ((uint32_t)h23.y << 16);
-    }
+__device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w, uint32_t sel) {
+  if constexpr (QK == 1) {
+    const uint32_t h = __byte_perm(w ^ 0x80808080u, 0x64646464u, sel);
+    const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t*>(&c);
+  } else {
+    // the same two bytes, packed into the low half-word, through the E4M3 -> f16x2 conversion
+    const uint32_t pair = __byte_perm(w, 0u, (sel & 0xfu) | ((sel & 0xf00u) >> 4));
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
   }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
+// selectors (result bytes 0 and 2 carry the codes; bytes 1 and 3 take 0x64 from the constant)
+constexpr uint32_t kSelB01 = 0x5140;  // codes in bytes 0, 1
+constexpr uint32_t kSelB23 = 0x5342;  // codes in bytes 2, 3
+constexpr uint32_t kSelB02 = 0x5240;  // codes in bytes 0, 2
+constexpr uint32_t kSelB13 = 0x5341;  // codes in bytes 1, 3
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low half)
@@ -239,26 +249,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return pack_f16x2(lo, hi);
 }
 
-// A 16-row tile of codes (kBoxes swizzled 128-byte columns) -> the 16-bit tile layout the MMA
-// path reads (kDChunks swizzled 128-byte columns), in fp16. Rows at or past `valid_rows` become
-// zeros.
-template <int D, int QK>
-__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int valid_rows, int lane) {
-  using C = DecCfg<D, QK>;
-  for (int idx = lane; idx < kChunk * C::kBoxes * 8; idx += 32) {
-    const int row = idx / (C::kBoxes * 8);
-    const int rest = idx - row * (C::kBoxes * 8);
-    const int box = rest >> 3, unit = rest & 7;  // codes 128 * box + 16 * unit .. + 15
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-    if (row < valid_rows) codes_to_f16<QK>(*reinterpret_cast<const uint4*>(src + box * (kChunk * 128) + swz128(row, unit)), lo, hi);
-    const int col = 128 * box + 16 * unit;  // first bf16 column written
-    uint8_t* d = dst + (col / 64) * C::kStageRegion;
-    const int u0 = (col % 64) / 8;
-    *reinterpret_cast<uint4*>(d + swz128(row, u0)) = lo;
-    *reinterpret_cast<uint4*>(d + swz128(row, u0 + 1)) = hi;
-  }
-}
-
 template <int D, int NT, int QK>
 __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
@@ -268,14 +258,13 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared window
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint8_t* staging = smem + C::kRingBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
   uint64_t* empty = full + C::kStages;
   float* merge_ml = reinterpret_cast<float*>(empty + C::kStages);  // [consumers][ROWS][2]
   float* scales = merge_ml + C::kConsumers * 16 * 2;                // [stages][32] (8-bit caches)
   float* merge_o = reinterpret_cast<float*>(smem);                 // aliases the ring after the loop
   __shared__ int s_timeout;
-  __shared__ int s_issued;
+  __shared__ int s_issued[C::kProducers];
 
   const int unit = blockIdx.x / p.num_splits;
   const int split = blockIdx.x - unit * p.num_splits;
@@ -288,11 +277,11 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   // now and the two memory latencies overlap. (A window that turns out to start later than
   // the split is simply reloaded.)
   int spec_base = -64, spec_page = -1;
-  if (warp == C::kConsumers && lane == 0) {
+  if (warp >= C::kConsumers && lane == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
   }
-  if (!p.varlen && warp == C::kConsumers) {
+  if (!p.varlen && warp >= C::kConsumers) {
     spec_base = split * p.chunks_per_split * kChunk / p.block_size;
     spec_page = spec_base + lane < p.max_blocks ? __ldg(p.block_tables + (size_t)unit * p.max_blocks + spec_base + lane)
                                                 : -1;
@@ -311,19 +300,20 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     }
     fence_barrier_init();
     s_timeout = 0;
-    s_issued = 0;
+    for (int w = 0; w < C::kProducers; ++w) s_issued[w] = 0;
   }
   __syncthreads();
 
-  if (warp == C::kConsumers) {
+  if (warp >= C::kConsumers) {
     // ---------------- producer: page-table walk + TMA (and, for 8-bit caches, the scales)
     if (n_mine > 0) {
       const int32_t* table = p.block_tables + (size_t)u.table_row * p.max_blocks;
       // page ids are fetched 32 at a time, one per lane, and handed out by shuffle: one
       // table-load latency per 32 pages instead of one per chunk
       int win_base = spec_base, my_page = spec_page;
+      const int pw = warp - C::kConsumers;
       int issued = 0;
-      for (int i = 0; i < n_mine; ++i) {
+      for (int i = pw; i < n_mine; i += C::kProducers) {
         const int stage = i % C::kStages;
         bool ok = true;
         if (i >= C::kStages) ok = mbar_wait(&empty[stage], ((i / C::kStages) - 1) & 1);
@@ -371,7 +361,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         }
         issued = i + 1;
       }
-      if (lane == 0) s_issued = issued;
+      if (lane == 0) s_issued[pw] = issued;
     }
   } else {
     // ---------------- consumers
@@ -389,11 +379,13 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + (size_t)n * D);
 #pragma unroll
         for (int kk = 0; kk < C::kMT; ++kk) {
-          qf[nt][kk][0] = (n < G) ? __ldg(qr + (kk * 16 + 2 * t4) / 2) : 0u;
-          qf[nt][kk][1] = (n < G) ? __ldg(qr + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
-          if constexpr (QK != 0) {  // the converted codes are fp16: so are the queries
-            qf[nt][kk][0] = bf16x2_to_f16x2(qf[nt][kk][0]);
-            qf[nt][kk][1] = bf16x2_to_f16x2(qf[nt][kk][1]);
+          if constexpr (QK == 0) {
+            qf[nt][kk][0] = (n < G) ? __ldg(qr + (kk * 16 + 2 * t4) / 2) : 0u;
+            qf[nt][kk][1] = (n < G) ? __ldg(qr + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
+          } else {
+            // the codes' k-slot order (dims 4t..4t+3 of each 16-dim step), converted to fp16
+            qf[nt][kk][0] = (n < G) ? bf16x2_to_f16x2(__ldg(qr + (kk * 16 + 4 * t4) / 2)) : 0u;
+            qf[nt][kk][1] = (n < G) ? bf16x2_to_f16x2(__ldg(qr + (kk * 16 + 4 * t4 + 2) / 2)) : 0u;
           }
         }
       }
@@ -412,9 +404,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     const int mi = lane >> 3, ri = lane & 7;
     const int k_key = ri + 8 * (mi & 1), k_unit = mi >> 1;  // K: (keys 0-7|8-15) x (unit u0|u0+1)
     const int v_key = ri + 8 * (mi >> 1), v_unit = mi & 1;  // V^T: (d 0-7|8-15) x (keys 0-7|8-15)
-    uint8_t* my_stage_k = staging + warp * (2 * C::kStagingTile);
-    uint8_t* my_stage_v = my_stage_k + C::kStagingTile;
-    constexpr int kRegionStride = QK ? C::kStageRegion : kChunk * 128;  // bytes between column halves
+    constexpr int kRegionStride = kChunk * 128;  // bytes between the 128-byte columns of a tile
 
     for (int i = warp; i < n_mine; i += C::kConsumers) {
       const int stage = i % C::kStages;
@@ -429,24 +419,56 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
       const int nvalid = min(kChunk, u.len - key0);
       const int nlow = u.start - key0;  // keys below this index of the chunk are outside the window
       float ks_a = 1.f, ks_b = 1.f, vs_a = 1.f, vs_b = 1.f;
+      // 8-bit caches: the chunk's codes go to registers (per thread 16 bytes of K and of V per
+      // 128 head dims) and the stage is released before any arithmetic; at D 256 the value codes
+      // are loaded after the scores, which keeps the two sets from being live together
+      uint32_t kw[QK ? C::kMT : 1][2], vw[QK ? C::kMT : 1][2];
+      // ldmatrix of matrices (keys 0-7 | 8-15) x (16-byte units u0 | u0+1) of 32 head dims
+      auto load_codes = [&](const uint8_t* tile, uint32_t (&w)[QK ? C::kMT : 1][2], bool trans) {
+#pragma unroll
+        for (int k2 = 0; k2 < C::kMT / 2; ++k2) {
+          const uint32_t off = (k2 >> 2) * kRegionStride + swz128(k_key, 2 * (k2 & 3) + k_unit);
+          uint32_t r[4];
+          if (trans) ldsm_x4_trans(r, smem_addr(tile + off)); else ldsm_x4(r, smem_addr(tile + off));
+          w[2 * k2][0] = r[0];
+          w[2 * k2][1] = r[1];
+          w[2 * k2 + 1][0] = r[2];
+          w[2 * k2 + 1][1] = r[3];
+        }
+      };
+      // value codes of keys past the sequence end (anything, NaN codes included) become 0, so
+      // 0-probability keys contribute exactly 0 to P.V; this thread holds keys 2t, 2t+1 (bytes
+      // 0-1, 2-3) of keys 0-7 and the same of keys 8-15
+      auto load_values_and_release = [&]() {
+        load_codes(vt, vw, true);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);  // the codes are in registers
+        if (nvalid < kChunk) {
+          const uint32_t m0 = (2 * t4 < nvalid ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nvalid ? 0xffff0000u : 0u);
+          const uint32_t m1 =
+              (2 * t4 + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * t4 + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < C::kMT; ++mt) {
+            vw[mt][0] &= m0;
+            vw[mt][1] &= m1;
+          }
+        }
+      };
+      constexpr bool kLateValues = QK != 0 && D > 128;
       if constexpr (QK != 0) {
         const float* sc = scales + stage * 32;
         ks_a = sc[g4];
         ks_b = sc[g4 + 8];
         vs_a = sc[16 + g4];
         vs_b = sc[16 + g4 + 8];
-        convert_tile<D, QK>(kt, my_stage_k, kChunk, lane);
-        convert_tile<D, QK>(vt, my_stage_v, nvalid, lane);  // rows past the end become zeros
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);  // the codes are no longer needed
-        kt = my_stage_k;
-        vt = my_stage_v;
+        load_codes(kt, kw, false);
+        if constexpr (!kLateValues) load_values_and_release();
       } else if (nvalid < kChunk) {
         // rows past the sequence end may hold anything (NaN included): zero them so that
         // 0-probability keys contribute exactly 0 to P.V (a select, not a multiply)
-        for (int idx = lane; idx < (kChunk - nvalid) * C::kDChunks * 8; idx += 32) {
-          const int row = nvalid + idx / (C::kDChunks * 8);
-          const int rest = idx % (C::kDChunks * 8);
+        for (int idx = lane; idx < (kChunk - nvalid) * (D / 64) * 8; idx += 32) {
+          const int row = nvalid + idx / ((D / 64) * 8);
+          const int rest = idx % ((D / 64) * 8);
           reinterpret_cast<uint4*>(vt + (rest / 8) * (kChunk * 128) + row * 128)[rest % 8] = make_uint4(0, 0, 0, 0);
         }
         // these generic-proxy writes precede the next TMA write of this stage
@@ -460,12 +482,20 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
 #pragma unroll
       for (int kk = 0; kk < C::kMT; ++kk) {
         uint32_t a[4];
-        const int dch = kk >> 2;
-        const int unit_idx = 2 * (kk & 3) + k_unit;
-        ldsm_x4(a, smem_addr(kt + dch * kRegionStride + swz128(k_key, unit_idx)));
+        if constexpr (QK == 0) {
+          const int dch = kk >> 2;
+          const int unit_idx = 2 * (kk & 3) + k_unit;
+          ldsm_x4(a, smem_addr(kt + dch * kRegionStride + swz128(k_key, unit_idx)));
+        } else {  // keys g, g+8 x k-slots (2t, 2t+1 | 2t+8, 2t+9) = dims (4t, 4t+1 | 4t+2, 4t+3)
+          a[0] = codes2_to_f16x2<QK>(kw[kk][0], kSelB01);
+          a[1] = codes2_to_f16x2<QK>(kw[kk][1], kSelB01);
+          a[2] = codes2_to_f16x2<QK>(kw[kk][0], kSelB23);
+          a[3] = codes2_to_f16x2<QK>(kw[kk][1], kSelB23);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_cache<QK>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
       }
+      if constexpr (kLateValues) load_values_and_release();
       // online softmax (rows 2*t4 and 2*t4+1; keys g4 and g4+8)
       uint32_t pb[NT][2];
 #pragma unroll
@@ -522,14 +552,21 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
 #pragma unroll
       for (int mt = 0; mt < C::kMT; ++mt) {
         uint32_t a[4];
-        const int dch = mt >> 2;
-        const int unit_idx = 2 * (mt & 3) + v_unit;
-        ldsm_x4_trans(a, smem_addr(vt + dch * kRegionStride + swz128(v_key, unit_idx)));
+        if constexpr (QK == 0) {
+          const int dch = mt >> 2;
+          const int unit_idx = 2 * (mt & 3) + v_unit;
+          ldsm_x4_trans(a, smem_addr(vt + dch * kRegionStride + swz128(v_key, unit_idx)));
+        } else {  // rows g, g+8 = dims 2g, 2g+1 of the block x keys (2t, 2t+1 | 2t+8, 2t+9)
+          a[0] = codes2_to_f16x2<QK>(vw[mt][0], kSelB02);
+          a[1] = codes2_to_f16x2<QK>(vw[mt][0], kSelB13);
+          a[2] = codes2_to_f16x2<QK>(vw[mt][1], kSelB02);
+          a[3] = codes2_to_f16x2<QK>(vw[mt][1], kSelB13);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_cache<QK>(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
-      __syncwarp();  // the staging tile (8-bit caches) is rewritten next iteration
       if constexpr (QK == 0) {
+        __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
       }
     }
@@ -553,8 +590,10 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         }
 #pragma unroll
         for (int mt = 0; mt < C::kMT; ++mt) {
-          merge_o[(warp * ROWS + n) * D + mt * 16 + g4] = o[nt][mt][j];
-          merge_o[(warp * ROWS + n) * D + mt * 16 + g4 + 8] = o[nt][mt][2 + j];
+          // accumulator rows g, g+8: dims g, g+8 (bf16) or 2g, 2g+1 (codes) of the block
+          const int d_lo = QK ? 2 * g4 : g4, d_hi = QK ? 2 * g4 + 1 : g4 + 8;
+          merge_o[(warp * ROWS + n) * D + mt * 16 + d_lo] = o[nt][mt][j];
+          merge_o[(warp * ROWS + n) * D + mt * 16 + d_hi] = o[nt][mt][2 + j];
         }
       }
     }
@@ -565,9 +604,11 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (s_timeout && threadIdx.x == C::kConsumers * 32) {
     // wind down: let copies still in flight land before the CTA's shared memory is released
-    const int issued = s_issued;
-    for (int i = max(0, issued - C::kStages); i < issued; ++i)
-      (void)mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1);
+    // chunk i went out iff its producer (i mod kProducers) got past it
+    int hi = 0;
+    for (int w = 0; w < C::kProducers; ++w) hi = max(hi, s_issued[w]);
+    for (int i = max(0, hi - C::kStages); i < hi; ++i)
+      if (i < s_issued[i % C::kProducers]) (void)mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1);
   }
   __syncthreads();
   merge_and_store<__nv_bfloat16>(p, merge_o, merge_ml, C::kConsumers, ROWS, D, unit, u.q_row, kvh, split);
