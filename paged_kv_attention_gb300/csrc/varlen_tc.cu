@@ -339,9 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
-    // ------------------------------------------------ producer (lane 0): Q_A, Q_B once, then K/V
-    // tiles. The page ids of tile i+1 are loaded while tile i's copies are issued and its
-    // stages wait to be freed, so no table load sits between two copies.
+    // ------------------------------------------------ producer (warp 8): Q_A, Q_B once, then K/V
+    // tiles. Lane k copies page k of a tile (its id loaded one tile ahead), so a tile's copies
+    // go out from up to 8 threads at once: one thread issuing them all is slower than HBM at
+    // small block sizes.
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
@@ -351,52 +352,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a)
           tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
                       q_start + tok0 + t * TOK);
-      const int32_t* table = p.block_tables + (size_t)(kPrefix ? 0 : r) * p.max_blocks;
-      // ids of tile i's pages (pages_per_tile <= 8 since the block size is >= 16)
-      auto load_ids = [&](int i, int (&ids)[8]) {
-        const int p0 = (j0 + i) * pages_per_tile;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ids[k] = (k < pages_per_tile && p0 + k < seq_pages) ? __ldg(table + p0 + k) : 0;
-      };
-      int cur[8], nxt[8];
-      load_ids(0, cur);
-      for (int i = 0; i < n_kv; ++i) {
-        const int st = i % kStages;
-        const uint32_t round_parity = ((i / kStages) - 1) & 1;
-        const int p0 = (j0 + i) * pages_per_tile;
-        const int np = min(p0 + pages_per_tile, seq_pages) - p0;
-        const uint32_t bytes = (uint32_t)np * bs * 256u;
-        if (i + 1 < n_kv) load_ids(i + 1, nxt);
-        if (i >= kStages && !wait_or_abort(&bars[B_KE + st], round_parity, abort_flag)) {
-          set_abort(abort_flag, p.err);
-          break;
-        }
-        mbar_arrive_expect_tx(&bars[B_KF + st], bytes);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k >= np) break;
-          if (cur[k] < 0 || cur[k] >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
-          for (int a = 0; a < 2; ++a)
-            tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + k * bs * 128, &kmap, &bars[B_KF + st],
-                        a * 64, kvh, 0, cur[k]);
-        }
-        if (i >= kStages && !wait_or_abort(&bars[B_VE + st], round_parity, abort_flag)) {
+    }
+    const int32_t* table = p.block_tables + (size_t)(kPrefix ? 0 : r) * p.max_blocks;
+    // this lane's page of tile i (pages_per_tile <= 8 since the block size is >= 16)
+    auto page_of = [&](int i) {
+      const int pg = (j0 + i) * pages_per_tile + lane;
+      return (lane < pages_per_tile && pg < seq_pages) ? __ldg(table + pg) : 0;
+    };
+    int cur = n_kv > 0 ? page_of(0) : 0;
+    for (int i = 0; i < n_kv; ++i) {
+      const int st = i % kStages;
+      const uint32_t round_parity = ((i / kStages) - 1) & 1;
+      const int p0 = (j0 + i) * pages_per_tile;
+      const int np = min(p0 + pages_per_tile, seq_pages) - p0;
+      const uint32_t bytes = (uint32_t)np * bs * 256u;
+      const int nxt = i + 1 < n_kv ? page_of(i + 1) : 0;
+      if (i >= kStages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
+        if (lane == 0) set_abort(abort_flag, p.err);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B_KF + st], bytes);
+      __syncwarp();
+      if (lane < np) {
+        if (cur < 0 || cur >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
+        for (int a = 0; a < 2; ++a)
+          tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st],
+                      a * 64, kvh, 0, cur);
+      }
+      if (i >= kStages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
+        if (lane == 0) {
           set_abort(abort_flag, p.err);
           *issued_tiles = i + 1;  // K of iteration i is in flight
-          break;
         }
-        mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k >= np) break;
-          for (int a = 0; a < 2; ++a)
-            tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + k * bs * 128, &vmap, &bars[B_VF + st],
-                        a * 64, kvh, 0, cur[k]);
-        }
-        *issued_tiles = i + 1;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) cur[k] = nxt[k];
+        break;
       }
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
+      __syncwarp();
+      if (lane < np)
+        for (int a = 0; a < 2; ++a)
+          tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st],
+                      a * 64, kvh, 0, cur);
+      __syncwarp();
+      if (lane == 0) *issued_tiles = i + 1;
+      cur = nxt;
     }
   } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer (lane 0); the warp zeroes V tails
