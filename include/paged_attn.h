@@ -106,12 +106,16 @@ int pa_supports(int is_varlen, int head_dim, int num_q_heads, int num_kv_heads,
 /* Split-count heuristic of the decode path (host only, no CUDA call).
  * Source: "32. Production attention kernels", Long contexts: split the keys (choose_splits:
  * enough programs to fill the GPU, no split smaller than a few blocks, at most 32), taken
- * further here: among the admissible counts, the one whose CTA count best fills whole waves
- * of `num_sms * ctas_per_sm` resident CTAs.
- *   num_units        = num_seqs * num_kv_heads (CTAs per split)
- *   max_chunks       = cdiv(max_blocks_per_seq * block_size, 16) (16-token chunks per row)
+ * further here: splits of at least `min_chunks_per_split` chunks are preferred (each CTA pays a
+ * fixed start-up and merge cost), and among those the count whose CTAs best fill whole waves
+ * of `num_sms * ctas_per_sm` resident CTAs; when such long splits leave less than one wave,
+ * the count that fills one wave (splits of at least 4 chunks).
+ *   num_units            = num_seqs * num_kv_heads (CTAs per split)
+ *   max_chunks           = cdiv(max_blocks_per_seq * block_size, 16) (16-token chunks per row)
+ *   min_chunks_per_split = preferred shortest split (the library uses 64 for bf16, 256 for
+ *                          8-bit caches); values below 4 act as 4
  * Returns a count in [1, 32]; 1 for degenerate inputs. */
-int pa_plan_decode_splits(int num_units, int max_chunks, int num_sms, int ctas_per_sm);
+int pa_plan_decode_splits(int num_units, int max_chunks, int num_sms, int ctas_per_sm, int min_chunks_per_split);
 
 /* The split count an auto (num_splits = 0) pa_paged_attention_decode call with these sizes
  * uses on the CURRENT device (queries the SM count and the kernel's occupancy once per

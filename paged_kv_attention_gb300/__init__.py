@@ -76,8 +76,9 @@ def supports(is_varlen: bool, head_dim: int, num_q_heads: int, num_kv_heads: int
                                         _DTYPES.get(dtype, -1)))
 
 
-def plan_decode_splits(num_units: int, max_chunks: int, num_sms: int, ctas_per_sm: int) -> int:
-    return _lib.load().pa_plan_decode_splits(num_units, max_chunks, num_sms, ctas_per_sm)
+def plan_decode_splits(num_units: int, max_chunks: int, num_sms: int, ctas_per_sm: int,
+                       min_chunks_per_split: int = 64) -> int:
+    return _lib.load().pa_plan_decode_splits(num_units, max_chunks, num_sms, ctas_per_sm, min_chunks_per_split)
 
 
 def decode_auto_splits(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,

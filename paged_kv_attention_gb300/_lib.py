@@ -40,7 +40,7 @@ SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i]),
     "pa_version": (_i, []),
     "pa_supports": (_i, [_i, _i, _i, _i, _i, _i]),
-    "pa_plan_decode_splits": (_i, [_i, _i, _i, _i]),
+    "pa_plan_decode_splits": (_i, [_i, _i, _i, _i, _i]),
     "pa_decode_auto_splits": (_i, [_i, _i, _i, _i, _i, _i, _i]),
     "pa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "pa_reshape_and_cache": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p]),

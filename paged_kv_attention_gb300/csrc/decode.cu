@@ -93,6 +93,9 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
   return u;
 }
 
+// Threshold of the lazy rescale (log2 units): probabilities against a stale reference are < 2^8.
+constexpr float kLazyRescale = 8.0f;
+
 // Score in log2 units: s * scale * log2 e, or with a softcap c: c * tanh(s * scale / c) * log2 e
 // ("poot - Attention and KV Cache", The streaming schedule: softcap_or_identity).
 __device__ __forceinline__ float score_log2(const DecodeParams& p, float s) {
@@ -523,22 +526,32 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+        // lazy rescaling: a row's reference maximum moves only when a score passes it by more
+        // than 2^8 (log2 units), so most chunks skip the accumulator rescale; (acc, m, l) stay
+        // consistent with whichever reference is kept, and probabilities stay below 2^8. The
+        // decision is the same in the 8 threads of a row (they share the row maximum).
+        const bool up0 = mx0 > m_run[nt][0] + kLazyRescale, up1 = mx1 > m_run[nt][1] + kLazyRescale;
+        const float mn0 = up0 ? mx0 : m_run[nt][0], mn1 = up1 ? mx1 : m_run[nt][1];
         const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-        const float al0 = exp2f(m_run[nt][0] - mu0), al1 = exp2f(m_run[nt][1] - mu1);
-        const float p0 = exp2f(x0 - mu0), p2 = exp2f(x2 - mu0);
-        const float p1 = exp2f(x1 - mu1), p3 = exp2f(x3 - mu1);
-        l_run[nt][0] = l_run[nt][0] * al0 + p0 + p2;
-        l_run[nt][1] = l_run[nt][1] * al1 + p1 + p3;
+        const float p0 = ex2_ftz(x0 - mu0), p2 = ex2_ftz(x2 - mu0);
+        const float p1 = ex2_ftz(x1 - mu1), p3 = ex2_ftz(x3 - mu1);
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+          const float al0 = up0 ? ex2_ftz(m_run[nt][0] - mu0) : 1.f;  // 2^-inf = 0 on the first keys
+          const float al1 = up1 ? ex2_ftz(m_run[nt][1] - mu1) : 1.f;
+          l_run[nt][0] *= al0;
+          l_run[nt][1] *= al1;
+#pragma unroll
+          for (int mt = 0; mt < C::kMT; ++mt) {
+            o[nt][mt][0] *= al0;
+            o[nt][mt][1] *= al1;
+            o[nt][mt][2] *= al0;
+            o[nt][mt][3] *= al1;
+          }
+        }
+        l_run[nt][0] += p0 + p2;
+        l_run[nt][1] += p1 + p3;
         m_run[nt][0] = mn0;
         m_run[nt][1] = mn1;
-#pragma unroll
-        for (int mt = 0; mt < C::kMT; ++mt) {
-          o[nt][mt][0] *= al0;
-          o[nt][mt][1] *= al1;
-          o[nt][mt][2] *= al0;
-          o[nt][mt][3] *= al1;
-        }
         // a value's scale multiplies its probabilities before P.V (the sums above stay unscaled)
         if constexpr (QK == 0) {
           pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7

@@ -125,25 +125,33 @@ extern "C" int pa_supports(int is_varlen, int head_dim, int num_q_heads, int num
   return 0;
 }
 
-extern "C" int pa_plan_decode_splits(int num_units, int max_chunks, int num_sms, int ctas_per_sm) {
+extern "C" int pa_plan_decode_splits(int num_units, int max_chunks, int num_sms, int ctas_per_sm,
+                                     int min_chunks_per_split) {
   if (num_units <= 0 || max_chunks <= 0 || num_sms <= 0 || ctas_per_sm <= 0) return 1;
-  // No split shorter than 4 chunks (64 tokens), none at all past 32, and never more splits
-  // than chunks (empty trailing splits would only cost the combine).
+  // Never a split under 4 chunks (64 tokens), none at all past 32, never more splits than
+  // chunks. Each CTA pays a fixed start-up and merge cost, so splits should be long: prefer
+  // splits of at least `min_chunks_per_split` chunks, unless that leaves less than one wave of
+  // resident CTAs, in which case split (down to 4 chunks) until one wave is filled.
   constexpr int kMinChunksPerSplit = 4;
-  const int cap = (int)std::max<long long>(1, std::min<long long>(kMaxSplits, max_chunks / kMinChunksPerSplit));
   const long long slots = (long long)num_sms * ctas_per_sm;
+  const long long cap = std::max<long long>(1, std::min<long long>(kMaxSplits, max_chunks / kMinChunksPerSplit));
+  const long long cap_long = std::max<long long>(1, std::min<long long>(cap, max_chunks / std::max(1, min_chunks_per_split)));
+  const long long fill = cdivll(slots, num_units);  // splits for one full wave
+  if (fill > cap_long) return (int)std::min<long long>(fill, cap);
+  // among the long enough counts, the one whose CTA count best fills whole waves; a larger
+  // count must fill them clearly better to win
   int best = 1;
   double best_eff = -1.0;
-  for (int s = 1; s <= cap; ++s) {
+  for (int sp = 1; sp <= cap_long; ++sp) {
     // splits whose boundaries fall on the same chunks are one choice: keep the smallest
-    const long long per = cdivll(max_chunks, s);
-    if (cdivll(max_chunks, per) != s) continue;
-    const long long ctas = (long long)num_units * s;
+    const long long per = cdivll(max_chunks, sp);
+    if (cdivll(max_chunks, per) != sp) continue;
+    const long long ctas = (long long)num_units * sp;
     const long long waves = cdivll(ctas, slots);
     const double eff = (double)ctas / (double)(waves * slots);
-    if (eff > best_eff + 0.02) {  // a larger count must fill waves clearly better to win
+    if (eff > best_eff + 0.02) {
       best_eff = eff;
-      best = s;
+      best = sp;
     }
   }
   return best;
@@ -204,6 +212,12 @@ pa_status validate_common(const void* q, const void* k_cache, const void* v_cach
   return PA_OK;
 }
 
+// Preferred shortest split, in 16-token chunks (measured on GB300 at 64 x 4096: bf16 calls ran
+// 171 us at the wave-filling 7 splits and 167 us at 3-4; 8-bit-code calls, limited by their
+// consumers rather than HBM, ran 160 us at 7 splits and 112 us at 1).
+constexpr int kMinChunksPerSplitBf16 = 64;
+constexpr int kMinChunksPerSplitCodes = 256;
+
 int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long max_chunks, pa_dtype dtype,
                 int quant = 0) {
   int occ;
@@ -216,7 +230,8 @@ int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long ma
     if (slot == 0) slot = decode_f32_ctas_per_sm(D, G);
     occ = slot;
   }
-  int s = pa_plan_decode_splits(units * Hkv, (int)std::min<long long>(max_chunks, 1 << 30), info->sms, occ);
+  int s = pa_plan_decode_splits(units * Hkv, (int)std::min<long long>(max_chunks, 1 << 30), info->sms, occ,
+                                quant != 0 ? kMinChunksPerSplitCodes : kMinChunksPerSplitBf16);
   s = (int)std::min<long long>(s, max_chunks);
   const long long per = cdivll(max_chunks, s);
   return (int)cdivll(max_chunks, per);

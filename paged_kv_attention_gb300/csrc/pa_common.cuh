@@ -117,6 +117,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// 2^x on the special-function unit (results below 2^-126 flush to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Fold a per-head sink logit z (natural-log units; it joins the softmax denominator and

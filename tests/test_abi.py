@@ -67,33 +67,40 @@ def test_supports(lib):
 
 class TestSplitPlanning:
     """pa_plan_decode_splits: the choose_splits rule of "32. Production attention kernels"
-    (Long contexts: split the keys) with a whole-wave criterion."""
+    (Long contexts: split the keys) with a preferred shortest split and a whole-wave criterion."""
 
     def test_degenerate_inputs_give_one(self, lib):
-        assert lib.pa_plan_decode_splits(0, 10, 152, 3) == 1
-        assert lib.pa_plan_decode_splits(4, 0, 152, 3) == 1
-        assert lib.pa_plan_decode_splits(4, 10, 0, 3) == 1
+        assert lib.pa_plan_decode_splits(0, 10, 152, 3, 64) == 1
+        assert lib.pa_plan_decode_splits(4, 0, 152, 3, 64) == 1
+        assert lib.pa_plan_decode_splits(4, 10, 0, 3, 64) == 1
 
     def test_bounds(self, lib):
         for units in (1, 2, 8, 32, 256, 512, 4096):
             for chunks in (1, 3, 4, 13, 64, 256, 2048):
-                s = lib.pa_plan_decode_splits(units, chunks, 152, 3)
-                assert 1 <= s <= 32
-                assert s <= max(1, chunks // 4)          # no split under 4 chunks
+                for min_chunks in (0, 4, 64, 256):
+                    s = lib.pa_plan_decode_splits(units, chunks, 152, 3, min_chunks)
+                    assert 1 <= s <= 32
+                    assert s <= max(1, chunks // 4)          # no split under 4 chunks
 
     def test_small_batch_long_context_splits(self, lib):
-        # 1 sequence x 2 KV heads over 256 chunks: many splits to fill 152 SMs
-        assert lib.pa_plan_decode_splits(2, 256, 152, 3) >= 16
+        # 1 sequence x 2 KV heads over 256 chunks: long splits cannot fill 152 SMs, so split
+        # down to one full wave (capped at 32)
+        assert lib.pa_plan_decode_splits(2, 256, 152, 3, 64) >= 16
+        assert lib.pa_plan_decode_splits(32, 256, 152, 2, 256) == 10   # 320 CTAs >= 304 slots
 
-    def test_fills_waves(self, lib):
-        # 64 x 8 units at 3 CTAs/SM: one split leaves the second wave 12% full
-        s = lib.pa_plan_decode_splits(512, 256, 152, 3)
-        ctas = 512 * s
-        waves = -(-ctas // 456)
-        assert ctas / (waves * 456) > 0.95
+    def test_long_splits_fill_waves(self, lib):
+        # 64 x 8 units over 256 chunks at 3 CTAs/SM: splits of >= 64 chunks allow 1-4; 4 fills
+        # its 5 waves best (90%)
+        s = lib.pa_plan_decode_splits(512, 256, 152, 3, 64)
+        assert s == 4
+        assert 256 // s >= 64
+
+    def test_enough_ctas_stay_whole(self, lib):
+        # one wave of CTAs already, and splits must cover >= 256 chunks: no split
+        assert lib.pa_plan_decode_splits(512, 256, 152, 2, 256) == 1
 
     def test_short_contexts_do_not_split(self, lib):
-        assert lib.pa_plan_decode_splits(4096, 4, 152, 3) == 1
+        assert lib.pa_plan_decode_splits(4096, 4, 152, 3, 64) == 1
 
 
 def test_workspace_bytes(lib):
