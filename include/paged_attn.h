@@ -302,9 +302,11 @@ pa_status pa_reshape_and_cache_quant(const void* key, const void* value, pa_dtyp
                                      int32_t* error_word, void* stream);
 
 /* Decode over an 8-bit cache: as pa_paged_attention_decode_ex (q and out bf16), with keys and
- * values dequantised in registers: codes are exact in bf16, a key's scale multiplies its
- * scores and a value's scale its probabilities before P.V. Supported: D in {128, 256},
- * Hq/Hkv <= 16, block_size % 16 == 0. */
+ * values dequantised in registers: codes are converted exactly to fp16 (every int8 code and
+ * every E4M3 value is an fp16 value) and the products run in fp16 with fp32 accumulation (q
+ * converted to fp16, probabilities rounded to fp16); a key's scale multiplies its scores and a
+ * value's scale its probabilities before P.V. Supported: D in {128, 256}, Hq/Hkv <= 16,
+ * block_size % 16 == 0. */
 pa_status pa_paged_attention_decode_quant(const void* q, const void* k_cache, const void* v_cache,
                                           const float* k_scales, const float* v_scales, pa_dtype cache_dtype,
                                           const int32_t* block_tables, const int32_t* context_lens,

@@ -20,6 +20,8 @@
 // from the limit; the point of the MMA is to keep the issue slots free for the memory
 // pipeline. The probabilities are moved from the score accumulator layout to the P.V
 // operand layout with movmatrix (an in-register 8x8 transpose), without shared memory.
+#include <atomic>
+
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -825,13 +827,15 @@ cudaError_t launch_tc_impl(const DecodeParams& p, const CUtensorMap& kmap, const
                            cudaStream_t stream) {
   using C = DecCfg<D, QK>;
   auto kern = decode_tc_kernel<D, NT, QK>;
-  static bool attr_done[64] = {};
+  // the shared-memory opt-in is per device; setting it again is harmless, so concurrent first
+  // calls from several host threads may both set it
+  static std::atomic<bool> attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
   dim3 grid((unsigned)(p.num_units * p.num_splits), (unsigned)p.num_kv_heads, 1);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, kmap, vmap);

@@ -1,6 +1,8 @@
 // C-ABI entry points: argument validation, split planning, TMA descriptor encoding and
 // launches on the caller's stream. Nothing here allocates device memory or synchronises.
 #include <math.h>
+
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -63,10 +65,12 @@ bool encode_query_map(CUtensorMap* map, const void* base, int D, int Hq, int N, 
   return r == CUDA_SUCCESS;
 }
 
+// Per-device facts, filled lazily. The occupancy slots are written by whichever host thread
+// first needs them (every writer stores the same value), so they are atomics.
 struct DeviceInfo {
   int sms = 0;
-  int occ_bf16[3][3][2] = {};  // [bf16 | int8 | fp8][D 64/128/256][group <= 8 | > 8]
-  int occ_f32[3][5] = {};   // [D][padded group 1..16]
+  std::atomic<int> occ_bf16[3][3][2] = {};  // [bf16 | int8 | fp8][D 64/128/256][group <= 8 | > 8]
+  std::atomic<int> occ_f32[3][5] = {};      // [D][padded group 1..16]
 };
 
 bool device_info(DeviceInfo** out) {
@@ -222,13 +226,19 @@ int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long ma
                 int quant = 0) {
   int occ;
   if (dtype == PA_DTYPE_BF16 || quant != 0) {
-    int& slot = info->occ_bf16[quant][dim_index(D)][G > 8 ? 1 : 0];
-    if (slot == 0) slot = decode_bf16_ctas_per_sm(D, G, quant);
-    occ = slot;
+    std::atomic<int>& slot = info->occ_bf16[quant][dim_index(D)][G > 8 ? 1 : 0];
+    occ = slot.load(std::memory_order_relaxed);
+    if (occ == 0) {
+      occ = decode_bf16_ctas_per_sm(D, G, quant);
+      slot.store(occ, std::memory_order_relaxed);
+    }
   } else {
-    int& slot = info->occ_f32[dim_index(D)][log2i(G)];
-    if (slot == 0) slot = decode_f32_ctas_per_sm(D, G);
-    occ = slot;
+    std::atomic<int>& slot = info->occ_f32[dim_index(D)][log2i(G)];
+    occ = slot.load(std::memory_order_relaxed);
+    if (occ == 0) {
+      occ = decode_f32_ctas_per_sm(D, G);
+      slot.store(occ, std::memory_order_relaxed);
+    }
   }
   int s = pa_plan_decode_splits(units * Hkv, (int)std::min<long long>(max_chunks, 1 << 30), info->sms, occ,
                                 quant != 0 ? kMinChunksPerSplitCodes : kMinChunksPerSplitBf16);

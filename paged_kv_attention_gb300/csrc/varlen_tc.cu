@@ -27,6 +27,8 @@
 //    reference max; this only bounds the range of P and O);
 //  * every wait is bounded; on expiry the CTA flags PA_ERRBIT_WAIT_TIMEOUT, drains its
 //    outstanding copies and MMAs, frees its tensor memory and exits.
+#include <atomic>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -682,15 +684,16 @@ int varlen_tc_tokens_per_cta(int group) { return 2 * (kBM / group); }
 
 cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {
-  static bool attr_done[64][2] = {};
+  // the shared-memory opt-in is per device and kernel; setting it twice is harmless
+  static std::atomic<bool> attr_done[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   const int mode = p.prefix_mode ? 1 : 0;
   auto kern = p.prefix_mode ? varlen_tc_kernel<true> : varlen_tc_kernel<false>;
-  if (dev < 64 && !attr_done[dev][mode]) {
+  if (dev < 0 || dev >= 64 || !attr_done[dev][mode].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev][mode] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev][mode].store(true, std::memory_order_release);
   }
   const long long ctas = (long long)p.q_tiles * p.num_reqs * p.num_kv_heads;
   if (ctas <= 0) return cudaSuccess;
