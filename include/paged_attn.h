@@ -241,6 +241,28 @@ pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const
                                        void* out, const pa_attn_options* options, int32_t* error_word,
                                        void* stream);
 
+/* pa_paged_attention_varlen_ex with a workspace. The same result; with a non-NULL workspace the
+ * batch's one-query (decode) requests are served by the split-KV decode (its splits keep long
+ * contexts streaming at HBM speed) and every other request by the tensor-core kernel; with NULL
+ * this is pa_paged_attention_varlen_ex. workspace: device memory of
+ * >= pa_varlen_workspace_bytes(...) bytes, 16-byte aligned, fully overwritten, not shared by
+ * calls that overlap on the GPU; PA_ERR_WORKSPACE_TOO_SMALL when it is shorter. Two launches
+ * (three with the decode's combine) on `stream`. */
+pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* query_start_loc, const int32_t* seq_lens,
+                                       const int32_t* block_tables,
+                                       int num_reqs, int num_tokens, int max_query_len,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int num_blocks, int max_blocks_per_seq,
+                                       int causal, float scale, pa_dtype dtype,
+                                       void* out, const pa_attn_options* options, void* workspace,
+                                       size_t workspace_bytes, int32_t* error_word, void* stream);
+
+/* Workspace bytes pa_paged_attention_varlen_ws needs (the split partials of num_reqs one-query
+ * requests at any split count; the decode bound of pa_decode_workspace_bytes). Host only. */
+size_t pa_varlen_workspace_bytes(int num_reqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
+                                 int block_size);
+
 /* Self-test of the bounded waits inside the kernels (failure detection without a fault): a
  * one-thread kernel waits, with a limit of limit_us microseconds (1..1,000,000), on a barrier
  * that nothing ever completes, then ORs PA_ERRBIT_WAIT_TIMEOUT into *error_word (a device

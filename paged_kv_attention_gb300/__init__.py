@@ -150,20 +150,32 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            scale: float | None = None, out: torch.Tensor | None = None,
                            error_word: torch.Tensor | None = None,
                            stream: torch.cuda.Stream | None = None, window: int = 0, softcap: float = 0.0,
-                           sinks: torch.Tensor | None = None) -> torch.Tensor:
+                           sinks: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           split_decodes: bool = False) -> torch.Tensor:
     """Flattened prefill / verify / decode batch; request r's queries are the newest q_len of
     its seq_lens[r] positions, causal by position. ``window``, ``softcap`` and ``sinks`` are
-    the pa_attn_options score modifiers."""
+    the pa_attn_options score modifiers. With ``split_decodes`` (bf16), the batch's one-query
+    requests go to the split-KV decode (a workspace is allocated unless one is given): faster
+    for batches that are mostly decodes, slower for prefill-heavy ones (two launches in turn
+    instead of one grid)."""
     n, hq, d = q.shape
     nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     r = seq_lens.shape[0]
     mb = block_tables.shape[1]
     if out is None:
         out = torch.empty_like(q)
-    st = _lib.load().pa_paged_attention_varlen_ex(
+    lib = _lib.load()
+    if split_decodes and q.dtype == torch.bfloat16 and workspace is None:
+        workspace = torch.empty(max(int(lib.pa_varlen_workspace_bytes(r, hq, d, mb, bs)), 16), dtype=torch.uint8,
+                                device=q.device)
+    if not split_decodes:
+        workspace = None
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.pa_paged_attention_varlen_ws(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
         r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
-        _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
+        _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(workspace), ws_len, _ptr(error_word),
+        _stream(stream))
     _check("pa_paged_attention_varlen", st)
     return out
 

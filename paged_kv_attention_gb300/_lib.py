@@ -63,6 +63,9 @@ SIGNATURES = {
                                              _i, _i, _i, _f, _p, _opt, _p, _p]),
     "pa_paged_attention_varlen_ex": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                           _i, _f, _i, _p, _opt, _p, _p]),
+    "pa_paged_attention_varlen_ws": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                          _i, _f, _i, _p, _opt, _p, _sz, _p, _p]),
+    "pa_varlen_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
 }
 
 _lib = None

@@ -47,16 +47,39 @@ struct Unit {
   int start;      // first visible position (> 0 only under a sliding window)
   int table_row;  // block table row
   int q_row;      // row of q / out
+  bool skip;      // not this launch's unit: write nothing
 };
 
 __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bool report) {
   Unit u;
+  u.skip = false;
   int len;
-  if (!p.varlen) {
+  if (p.varlen == 0) {
     u.table_row = unit;
     u.q_row = unit;
     len = p.context_lens[unit];
     u.start = 0;
+  } else if (p.varlen == 2) {
+    // a varlen request served only if it has exactly one query, at its newest position: it then
+    // sees all seq_len keys, causal or not (the tensor-core kernel takes every other request)
+    const int start = p.query_start_loc[unit];
+    const int stop = p.query_start_loc[unit + 1];
+    u.table_row = unit;
+    u.q_row = start;
+    u.start = 0;
+    if (stop - start != 1 || start < 0) {
+      u.skip = true;
+      len = 0;
+    } else {
+      len = p.seq_lens[unit];
+      if (len < 1) {  // the query's own position is not cached: a layout error, zero row
+        if (report) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
+        len = 0;
+      } else if (len > p.max_blocks * p.block_size) {  // as the varlen kernels: zero row, flag
+        if (report) flag_error(p.err, PA_ERRBIT_LENGTH_OUT_OF_RANGE);
+        len = 0;
+      }
+    }
   } else {
     // request r with query_start_loc[r] <= unit < query_start_loc[r+1]
     int lo = 0, hi = p.num_reqs;
@@ -90,7 +113,7 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
   }
   u.len = len;
   // decode: the query is the newest cached position, len - 1
-  if (!p.varlen && p.window > 0) u.start = max(0, len - p.window);
+  if (p.varlen != 1 && p.window > 0) u.start = max(0, len - p.window);
   if (u.start > u.len) u.start = u.len;
   return u;
 }
@@ -277,7 +300,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Decode (one query per sequence): the block-table row is the unit, and this split's first
+  // Decode (one query per unit): the block-table row is the unit, and this split's first
   // page is known before its length is, so the producer starts its first page-id window load
   // now and the two memory latencies overlap. (A window that turns out to start later than
   // the split is simply reloaded.)
@@ -286,12 +309,13 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
   }
-  if (!p.varlen && warp >= C::kConsumers) {
+  if (p.varlen != 1 && warp >= C::kConsumers) {
     spec_base = split * p.chunks_per_split * kChunk / p.block_size;
     spec_page = spec_base + lane < p.max_blocks ? __ldg(p.block_tables + (size_t)unit * p.max_blocks + spec_base + lane)
                                                 : -1;
   }
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
+  if (u.skip) return;  // uniform: another kernel serves this unit
   const int n_chunks = (u.len + kChunk - 1) / kChunk;
   const int c_begin = max(split * p.chunks_per_split, u.start / kChunk);
   const int c_end = min(n_chunks, split * p.chunks_per_split + p.chunks_per_split);
@@ -657,6 +681,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
+  if (u.skip) return;
   const int k_begin = max(split * p.chunks_per_split * kChunk, u.start);
   const int k_end = min(u.len, split * p.chunks_per_split * kChunk + p.chunks_per_split * kChunk);
 
@@ -771,6 +796,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   const int unit = gw / p.num_q_heads;
   const int h = gw - unit * p.num_q_heads;
   const int S = p.num_splits;
+  // the unit's output row (request units: only one-query requests were served, at their query)
+  int q_row = unit;
+  if (p.varlen == 2) {
+    q_row = p.query_start_loc[unit];
+    if (p.query_start_loc[unit + 1] - q_row != 1 || q_row < 0) return;
+  }
   const int D = p.head_dim;
   const size_t base = (size_t)unit * S * p.num_q_heads + h;  // slot of split s: base + s * Hq
   const float m_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2] : -INFINITY;
@@ -788,7 +819,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   L += exp2f(z2 - Mu);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)unit * p.num_q_heads + h) * D;
+  OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)q_row * p.num_q_heads + h) * D;
   // every lane runs every iteration (the weight shuffles need the whole warp); lanes past
   // the head dim only skip their loads and stores. Sixteen partials' loads are issued before
   // any of them is used, so their latencies overlap.

@@ -395,6 +395,11 @@ extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cach
                                       error_word, stream);
 }
 
+extern "C" size_t pa_varlen_workspace_bytes(int num_reqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
+                                            int block_size) {
+  return pa_decode_workspace_bytes(num_reqs, num_q_heads, head_dim, max_blocks_per_seq, block_size, 0);
+}
+
 extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
                                                   const int32_t* query_start_loc, const int32_t* seq_lens,
                                                   const int32_t* block_tables, int num_reqs, int num_tokens,
@@ -403,6 +408,20 @@ extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_c
                                                   int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
                                                   void* out, const pa_attn_options* options, int32_t* error_word,
                                                   void* stream) {
+  return pa_paged_attention_varlen_ws(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, num_reqs,
+                                      num_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      num_blocks, max_blocks_per_seq, causal, scale, dtype, out, options, nullptr, 0,
+                                      error_word, stream);
+}
+
+extern "C" pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_cache, const void* v_cache,
+                                                  const int32_t* query_start_loc, const int32_t* seq_lens,
+                                                  const int32_t* block_tables, int num_reqs, int num_tokens,
+                                                  int max_query_len, int num_q_heads, int num_kv_heads,
+                                                  int head_dim, int block_size, int num_blocks,
+                                                  int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
+                                                  void* out, const pa_attn_options* options, void* workspace,
+                                                  size_t workspace_bytes, int32_t* error_word, void* stream) {
   if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_reqs == 0 || num_tokens == 0) return PA_OK;
   if (!query_start_loc || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
@@ -415,7 +434,39 @@ extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_c
   cudaStream_t s = as_stream(stream);
 
   if (dtype == PA_DTYPE_BF16 && varlen_tc_supported(head_dim, G, block_size) && max_query_len > 0) {
+    // With a workspace, the one-query (decode) requests of the batch go to the split-KV decode,
+    // whose splits keep long contexts streaming at HBM speed; a 128-row tensor-core tile would
+    // carry G valid rows for them. The tensor-core kernel takes every other request.
+    const bool split_decodes = workspace != nullptr;
+    if (split_decodes) {
+      DecodeParams dp{};
+      dp.q = q;
+      dp.k_cache = k_cache;
+      dp.v_cache = v_cache;
+      dp.block_tables = block_tables;
+      dp.query_start_loc = query_start_loc;
+      dp.seq_lens = seq_lens;
+      dp.out = out;
+      dp.err = error_word;
+      dp.varlen = 2;
+      dp.causal = causal ? 1 : 0;
+      dp.num_reqs = num_reqs;
+      dp.num_units = num_reqs;
+      dp.num_q_heads = num_q_heads;
+      dp.num_kv_heads = num_kv_heads;
+      dp.group = G;
+      dp.head_dim = head_dim;
+      dp.block_size = block_size;
+      dp.num_blocks = num_blocks;
+      dp.max_blocks = max_blocks_per_seq;
+      dp.scale_log2 = sc * kLog2e;
+      st = apply_options(options, sc, dp);
+      if (st != PA_OK) return st;
+      st = run_decode_units(dp, PA_DTYPE_BF16, k_cache, v_cache, 0, workspace, workspace_bytes, s);
+      if (st != PA_OK) return st;
+    }
     VarlenParams vp{};
+    vp.skip_single = split_decodes ? 1 : 0;
     vp.query_start_loc = query_start_loc;
     vp.seq_lens = seq_lens;
     vp.block_tables = block_tables;

@@ -28,6 +28,8 @@ struct DecodeParams {
   float* ws_acc;  // [units, splits, Hq, D] when num_splits > 1
   float* ws_ml;   // [units, splits, Hq, 2]
   int32_t* err;
+  // units: 0 = sequences (decode); 1 = the query tokens of varlen requests; 2 = varlen requests,
+  // only those with exactly one query (the others are skipped: nothing is written for them)
   int varlen;
   int causal;
   int num_reqs;
@@ -110,6 +112,8 @@ struct VarlenParams {
   // slot t * slot_count + r of ws_acc / ws_ml instead of `out`
   int prefix_mode;
   const int32_t* prefix_len;
+  // requests with exactly one query are left to the split-KV decode (launched beside this kernel)
+  int skip_single;
   int prefix_tiles_per_split;
   float* ws_acc;
   float* ws_ml;

@@ -147,3 +147,37 @@ def test_cuda_graph_replay_follows_device_positions():
         want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, new, case.block_tables, True,
                                              case.scale)
         check_close(out, want, torch.bfloat16, label=f"varlen graph step {step}")
+
+
+@pytest.mark.parametrize("split_decodes", [True, False])
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 1, 64), (8, 8, 16)])
+def test_one_query_requests_on_either_path(split_decodes, hq, hkv, bs):
+    """One-query requests are served by the split-KV decode (with a workspace) or by the
+    tensor-core kernel (without); both agree with the oracle, long contexts included."""
+    q_lens = [1, 64, 1, 5, 1, 1, 200, 1]
+    seq_lens = [3000, 100, 1, 900, 4096, 17, 700, 2500]
+    case = workloads.make_case("v1q", 97 + hq + bs, q_lens, seq_lens, num_q_heads=hq, num_kv_heads=hkv,
+                               head_dim=128, block_size=bs, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    out = run_varlen(case, kc, vc, split_decodes=split_decodes)
+    rows = sample_tokens(case)
+    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), torch.bfloat16, rows=rows,
+                label=f"split_decodes={split_decodes} G{hq // hkv} bs{bs}")
+
+
+def test_one_query_request_without_its_position_is_flagged():
+    case = workloads.make_case("v1e", 98, [1, 3], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    lens = case.seq_lens.clone()
+    lens[0] = 0                                       # the query's own position is not cached
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pa.paged_attention_varlen(case.q.to(DEV), kc, vc, case.query_start_loc.to(DEV), lens.to(DEV),
+                                    case.block_tables.to(DEV), case.max_query_len, True, case.scale,
+                                    error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa._lib.PA_ERRBIT_QUERY_LAYOUT
+    assert torch.equal(out[:1].float(), torch.zeros_like(out[:1].float()))
+    ko, vo = oracle_pools(case)
+    check_close(out[1:], oracle_varlen(case, ko, vo)[1:], torch.bfloat16, label="clean request")
