@@ -217,8 +217,9 @@ pa_status validate_common(const void* q, const void* k_cache, const void* v_cach
 }
 
 // Preferred shortest split, in 16-token chunks (measured on GB300 at 64 x 4096: bf16 calls ran
-// 171 us at the wave-filling 7 splits and 167 us at 3-4; 8-bit-code calls, limited by their
-// consumers rather than HBM, ran 160 us at 7 splits and 112 us at 1).
+// 171 us at the wave-filling 7 splits and 167 us at 3-4; int8-code calls, limited by their
+// consumers rather than HBM, 160 us at 7 splits and 112 us at 1; fp8-code calls 169 us at 7,
+// 148 us at 1).
 constexpr int kMinChunksPerSplitBf16 = 64;
 constexpr int kMinChunksPerSplitCodes = 256;
 
