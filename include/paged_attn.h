@@ -92,6 +92,20 @@ typedef struct pa_attn_options {
   const float* sinks;
 } pa_attn_options;
 
+/* Row strides for the *_strided entry points, in ELEMENTS of the tensor's dtype (a NULL pointer,
+ * or 0 in a field, means dense rows of Hq * D elements).
+ *   q:   elements from one query row to the next (a sequence for decode, a token for varlen),
+ *        e.g. (Hq + 2 * Hkv) * D when q is the query slice of a fused QKV projection output;
+ *   out: likewise for the output rows.
+ * Within a row the Hq heads stay dense (D elements apart). A non-zero stride must be at least
+ * Hq * D (rows never overlap) and a whole number of 16-byte units (a multiple of 8 elements for
+ * bf16, 4 for f32), else PA_ERR_INVALID_ARGUMENT. The pages pass dense tensors; the strided form
+ * takes the row layouts a serving engine's projections produce without a copy. */
+typedef struct pa_row_strides {
+  int64_t q;
+  int64_t out;
+} pa_row_strides;
+
 /* Human-readable name of a status code. Never NULL. */
 const char* pa_status_string(int status);
 
@@ -142,6 +156,15 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
                                const int32_t* slot_mapping, int num_tokens,
                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                pa_dtype dtype, int32_t* error_word, void* stream);
+
+/* reshape_and_cache with strided key/value rows: key row i starts key_row_stride elements after
+ * row i - 1 (value likewise; 0 = dense, Hkv * D). Strides follow the pa_row_strides rules with
+ * Hkv * D in place of Hq * D; everything else is pa_reshape_and_cache. */
+pa_status pa_reshape_and_cache_strided(const void* key, const void* value, int64_t key_row_stride,
+                                       int64_t value_row_stride, void* k_cache, void* v_cache,
+                                       const int32_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                       int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                                       int32_t* error_word, void* stream);
 
 /* paged_attention_decode: one query per sequence, split-KV.
  * out[s, h] = softmax_p(scale * q[s,h] . K[s,p]) . V[s,p] over p in [0, context_lens[s]),
@@ -229,6 +252,16 @@ pa_status pa_paged_attention_decode_ex(const void* q, const void* k_cache, const
                                        void* out, void* workspace, size_t workspace_bytes,
                                        const pa_attn_options* options, int32_t* error_word, void* stream);
 
+/* pa_paged_attention_decode_ex with strided q / out rows (see pa_row_strides; NULL = dense). */
+pa_status pa_paged_attention_decode_strided(const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables, const int32_t* context_lens,
+                                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int num_blocks, int max_blocks_per_seq,
+                                            float scale, pa_dtype dtype, int num_splits,
+                                            void* out, void* workspace, size_t workspace_bytes,
+                                            const pa_attn_options* options, const pa_row_strides* strides,
+                                            int32_t* error_word, void* stream);
+
 /* pa_paged_attention_varlen with score modifiers (see pa_attn_options; NULL = none). All other
  * arguments, layouts and rules are those of pa_paged_attention_varlen. */
 pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -257,6 +290,19 @@ pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_cache, const
                                        int causal, float scale, pa_dtype dtype,
                                        void* out, const pa_attn_options* options, void* workspace,
                                        size_t workspace_bytes, int32_t* error_word, void* stream);
+
+/* pa_paged_attention_varlen_ws with strided q / out token rows (see pa_row_strides; NULL = dense).
+ * The tensor-core path reads q through a tensor map whose token stride is strides->q. */
+pa_status pa_paged_attention_varlen_strided(const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* query_start_loc, const int32_t* seq_lens,
+                                            const int32_t* block_tables,
+                                            int num_reqs, int num_tokens, int max_query_len,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int num_blocks, int max_blocks_per_seq,
+                                            int causal, float scale, pa_dtype dtype,
+                                            void* out, const pa_attn_options* options,
+                                            const pa_row_strides* strides, void* workspace,
+                                            size_t workspace_bytes, int32_t* error_word, void* stream);
 
 /* Workspace bytes pa_paged_attention_varlen_ws needs (the split partials of num_reqs one-query
  * requests at any split count; the decode bound of pa_decode_workspace_bytes). Host only. */

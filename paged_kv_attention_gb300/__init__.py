@@ -60,6 +60,23 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr()
 
 
+def _row_ptr(t: torch.Tensor) -> tuple[int, int]:
+    """(data pointer, row stride in elements) of a [rows, heads, D] tensor whose heads and head
+    dims are dense and whose rows may sit further apart (e.g. a slice of a fused QKV output)."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("rows of [rows, heads, head_dim] must hold their heads densely")
+    if t.shape[0] > 1 and t.stride(0) < t.shape[1] * t.shape[2]:
+        raise ValueError("rows must not overlap")
+    return t.data_ptr(), (t.stride(0) if t.shape[0] > 1 else t.shape[1] * t.shape[2])
+
+
+def _strides(q: torch.Tensor, out: torch.Tensor):
+    """pa_row_strides for the *_strided calls, or None when q and out are dense."""
+    if q.is_contiguous() and out.is_contiguous():
+        return None
+    return ctypes.byref(_lib.RowStrides(_row_ptr(q)[1], _row_ptr(out)[1]))
+
+
 def _stream(stream: torch.cuda.Stream | None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -106,13 +123,21 @@ def _options(window: int, softcap: float, sinks: torch.Tensor | None):
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       slot_mapping: torch.Tensor, error_word: torch.Tensor | None = None,
                       stream: torch.cuda.Stream | None = None) -> None:
-    """k_cache[slot // bs, slot % bs] = key[i] for slot = slot_mapping[i] >= 0 (same for v)."""
+    """k_cache[slot // bs, slot % bs] = key[i] for slot = slot_mapping[i] >= 0 (same for v).
+    key and value may be row-strided views (heads dense within a row)."""
     n, hkv, d = key.shape
     nb, bs = k_cache.shape[0], k_cache.shape[1]
-    st = _lib.load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
-                                          _ptr(slot_mapping), n, hkv, d, bs, nb, _dtype(key),
-                                          _ptr(error_word), _stream(stream))
-    _check("pa_reshape_and_cache", st)
+    if key.is_contiguous() and value.is_contiguous():
+        st = _lib.load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                              _ptr(slot_mapping), n, hkv, d, bs, nb, _dtype(key),
+                                              _ptr(error_word), _stream(stream))
+        _check("pa_reshape_and_cache", st)
+        return
+    (kp, ks), (vp, vs) = _row_ptr(key), _row_ptr(value)
+    st = _lib.load().pa_reshape_and_cache_strided(kp, vp, ks, vs, _ptr(k_cache), _ptr(v_cache),
+                                                  _ptr(slot_mapping), n, hkv, d, bs, nb, _dtype(key),
+                                                  _ptr(error_word), _stream(stream))
+    _check("pa_reshape_and_cache_strided", st)
 
 
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -136,10 +161,19 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.load().pa_paged_attention_decode_ex(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
-        s, hq, hkv, d, bs, nb, mb, float(scale or 0.0), _dtype(q), int(num_splits),
-        _ptr(out), _ptr(workspace), ws_len, _options(window, softcap, sinks), _ptr(error_word), _stream(stream))
+    strides = _strides(q, out)
+    if strides is None:
+        st = _lib.load().pa_paged_attention_decode_ex(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+            s, hq, hkv, d, bs, nb, mb, float(scale or 0.0), _dtype(q), int(num_splits),
+            _ptr(out), _ptr(workspace), ws_len, _options(window, softcap, sinks), _ptr(error_word),
+            _stream(stream))
+    else:
+        st = _lib.load().pa_paged_attention_decode_strided(
+            _row_ptr(q)[0], _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+            s, hq, hkv, d, bs, nb, mb, float(scale or 0.0), _dtype(q), int(num_splits),
+            _row_ptr(out)[0], _ptr(workspace), ws_len, _options(window, softcap, sinks), strides,
+            _ptr(error_word), _stream(stream))
     _check("pa_paged_attention_decode", st)
     return out
 
@@ -171,11 +205,19 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if not split_decodes:
         workspace = None
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.pa_paged_attention_varlen_ws(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
-        r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
-        _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(workspace), ws_len, _ptr(error_word),
-        _stream(stream))
+    strides = _strides(q, out)
+    if strides is None:
+        st = lib.pa_paged_attention_varlen_ws(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
+            r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),
+            _dtype(q), _ptr(out), _options(window, softcap, sinks), _ptr(workspace), ws_len, _ptr(error_word),
+            _stream(stream))
+    else:
+        st = lib.pa_paged_attention_varlen_strided(
+            _row_ptr(q)[0], _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+            _ptr(block_tables), r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)),
+            float(scale or 0.0), _dtype(q), _row_ptr(out)[0], _options(window, softcap, sinks), strides,
+            _ptr(workspace), ws_len, _ptr(error_word), _stream(stream))
     _check("pa_paged_attention_varlen", st)
     return out
 

@@ -35,6 +35,15 @@ class AttnOptions(ctypes.Structure):
 
 _opt = ctypes.POINTER(AttnOptions)
 
+
+class RowStrides(ctypes.Structure):
+    """pa_row_strides: elements from one q row / out row to the next (0 = dense)."""
+    _fields_ = [("q", ctypes.c_int64), ("out", ctypes.c_int64)]
+
+
+_rs = ctypes.POINTER(RowStrides)
+_i64 = ctypes.c_int64
+
 # name -> (restype, argtypes); mirrors include/paged_attn.h
 SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i]),
@@ -66,6 +75,11 @@ SIGNATURES = {
     "pa_paged_attention_varlen_ws": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                           _i, _f, _i, _p, _opt, _p, _sz, _p, _p]),
     "pa_varlen_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "pa_reshape_and_cache_strided": (_i, [_p, _p, _i64, _i64, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p]),
+    "pa_paged_attention_decode_strided": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                                               _p, _p, _sz, _opt, _rs, _p, _p]),
+    "pa_paged_attention_varlen_strided": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                               _i, _f, _i, _p, _opt, _rs, _p, _sz, _p, _p]),
 }
 
 _lib = None

@@ -152,7 +152,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, const flo
       if (p.sinks != nullptr) O *= fold_sink(p.sinks[h0 + n], M, L);
       const float v = (L > 0.f) ? O / L : 0.f;
       OutT* out = reinterpret_cast<OutT*>(p.out);
-      out[((size_t)q_row * p.num_q_heads + h0 + n) * D + d] = static_cast<OutT>(v);
+      out[(size_t)q_row * p.out_stride + (size_t)(h0 + n) * D + d] = static_cast<OutT>(v);
     } else {
       const size_t slot = ((size_t)unit * p.slot_count + p.slot_offset + split) * p.num_q_heads + h0 + n;
       p.ws_acc[slot * D + d] = O;
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     uint32_t qf[NT][C::kMT][2];
     {
       const __nv_bfloat16* qb =
-          reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)u.q_row * p.num_q_heads + (size_t)kvh * G) * D;
+          reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)u.q_row * p.q_stride + (size_t)kvh * G * D;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g4;
@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
   const int k_begin = max(split * p.chunks_per_split * kChunk, u.start);
   const int k_end = min(u.len, split * p.chunks_per_split * kChunk + p.chunks_per_split * kChunk);
 
-  const float* qg = reinterpret_cast<const float*>(p.q) + ((size_t)u.q_row * p.num_q_heads + (size_t)kvh * G) * D;
+  const float* qg = reinterpret_cast<const float*>(p.q) + (size_t)u.q_row * p.q_stride + (size_t)kvh * G * D;
   for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) q_s[idx] = (idx / D < G) ? qg[idx] : 0.f;
   __syncthreads();
 
@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   L += exp2f(z2 - Mu);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  OutT* out = reinterpret_cast<OutT*>(p.out) + ((size_t)q_row * p.num_q_heads + h) * D;
+  OutT* out = reinterpret_cast<OutT*>(p.out) + (size_t)q_row * p.out_stride + (size_t)h * D;
   // every lane runs every iteration (the weight shuffles need the whole warp); lanes past
   // the head dim only skip their loads and stores. Sixteen partials' loads are issued before
   // any of them is used, so their latencies overlap.
@@ -915,13 +915,22 @@ int pad_group(int g) {
   return gp;
 }
 
+// q / out row strides default to dense rows
+DecodeParams with_row_strides(const DecodeParams& in) {
+  DecodeParams p = in;
+  if (p.q_stride == 0) p.q_stride = (long long)p.num_q_heads * p.head_dim;
+  if (p.out_stride == 0) p.out_stride = (long long)p.num_q_heads * p.head_dim;
+  return p;
+}
+
 }  // namespace
 
 #define PA_TC_NT(D, QK) \
   (p.group > 8 ? launch_tc_impl<D, 2, QK>(p, kmap, vmap, stream) : launch_tc_impl<D, 1, QK>(p, kmap, vmap, stream))
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+cudaError_t launch_decode_bf16(const DecodeParams& p_in, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream) {
+  const DecodeParams p = with_row_strides(p_in);
   switch (p.quant * 1000 + p.head_dim) {
     case 64: return PA_TC_NT(64, 0);
     case 128: return PA_TC_NT(128, 0);
@@ -960,7 +969,8 @@ int decode_bf16_ctas_per_sm(int head_dim, int group, int quant) {
     default: return cudaErrorInvalidValue;                      \
   }
 
-cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_f32(const DecodeParams& p_in, cudaStream_t stream) {
+  const DecodeParams p = with_row_strides(p_in);
   switch (p.head_dim) {
     case 64: PA_F32_CASES(64)
     case 128: PA_F32_CASES(128)
@@ -988,7 +998,8 @@ int decode_f32_ctas_per_sm(int head_dim, int group) {
   }
 }
 
-cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
+cudaError_t launch_combine(const DecodeParams& p_in, pa_dtype dtype, cudaStream_t stream) {
+  const DecodeParams p = with_row_strides(p_in);
   const long long warps = (long long)p.num_units * p.num_q_heads;
   const unsigned blocks = (unsigned)((warps + 3) / 4);
   // programmatic dependent launch: the combine's CTAs launch while the split kernel's last CTAs

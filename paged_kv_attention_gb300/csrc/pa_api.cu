@@ -51,12 +51,14 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs
   return r == CUDA_SUCCESS;
 }
 
-// q [N, Hq, D] bf16 viewed as (D, Hq, N); one box = `tokens` tokens x `group` heads x 64 cols.
-bool encode_query_map(CUtensorMap* map, const void* base, int D, int Hq, int N, int group, int tokens) {
+// q [N, Hq, D] bf16 (rows row_stride elements apart) viewed as (D, Hq, N); one box = `tokens`
+// tokens x `group` heads x 64 cols.
+bool encode_query_map(CUtensorMap* map, const void* base, int D, int Hq, int N, int group, int tokens,
+                      long long row_stride) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)N};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)row_stride * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)tokens};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -99,6 +101,18 @@ bool group_ok_bf16(int G) { return G >= 1 && G <= 16; }
 bool group_ok_f32(int G, int D) { return G >= 1 && G <= 16 && G * D <= 2048; }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// A caller's row stride in elements: 0 = dense rows; otherwise at least a dense row (rows never
+// overlap) and a whole number of 16-byte units, so every row stays 16-byte aligned.
+bool resolve_row_stride(long long given, long long dense, int elt, long long* out) {
+  if (given == 0) {
+    *out = dense;
+    return true;
+  }
+  if (given < dense || (given * elt) % 16 != 0 || given > (1ll << 36)) return false;
+  *out = given;
+  return true;
+}
 
 }  // namespace
 }  // namespace pa
@@ -180,6 +194,15 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, vo
                                           const int32_t* slot_mapping, int num_tokens, int num_kv_heads,
                                           int head_dim, int block_size, int num_blocks, pa_dtype dtype,
                                           int32_t* error_word, void* stream) {
+  return pa_reshape_and_cache_strided(key, value, 0, 0, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                                      head_dim, block_size, num_blocks, dtype, error_word, stream);
+}
+
+extern "C" pa_status pa_reshape_and_cache_strided(const void* key, const void* value, int64_t key_row_stride,
+                                                  int64_t value_row_stride, void* k_cache, void* v_cache,
+                                                  const int32_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                                  int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                                                  int32_t* error_word, void* stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARGUMENT;
   if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
@@ -190,9 +213,15 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, vo
   const int elem = dtype == PA_DTYPE_BF16 ? 2 : 4;
   const long long row_bytes = (long long)num_kv_heads * head_dim * elem;
   if (row_bytes % 16 != 0 || row_bytes > (1ll << 30)) return PA_ERR_UNSUPPORTED;
+  const long long row_elems = (long long)num_kv_heads * head_dim;
+  long long key_stride = 0, value_stride = 0;
+  if (!resolve_row_stride(key_row_stride, row_elems, elem, &key_stride) ||
+      !resolve_row_stride(value_row_stride, row_elems, elem, &value_stride))
+    return PA_ERR_INVALID_ARGUMENT;
   const long long num_slots = (long long)num_blocks * block_size;
   cudaError_t e = launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, (int)row_bytes,
-                                           num_slots, error_word, as_stream(stream));
+                                           key_stride * elem, value_stride * elem, num_slots, error_word,
+                                           as_stream(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -329,6 +358,15 @@ pa_status apply_options(const pa_attn_options* o, float scale, Params& p) {
   return PA_OK;
 }
 
+// The q / out row strides of a pa_row_strides (NULL = dense rows), checked.
+bool resolve_strides(const pa_row_strides* st, int num_q_heads, int head_dim, pa_dtype dtype, long long* q_stride,
+                     long long* out_stride) {
+  const long long dense = (long long)num_q_heads * head_dim;
+  const int elt = dtype == PA_DTYPE_F32 ? 4 : 2;
+  return resolve_row_stride(st ? st->q : 0, dense, elt, q_stride) &&
+         resolve_row_stride(st ? st->out : 0, dense, elt, out_stride);
+}
+
 }  // namespace
 
 extern "C" pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -351,12 +389,29 @@ extern "C" pa_status pa_paged_attention_decode_ex(const void* q, const void* k_c
                                                   void* workspace, size_t workspace_bytes,
                                                   const pa_attn_options* options, int32_t* error_word,
                                                   void* stream) {
+  return pa_paged_attention_decode_strided(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                                           num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
+                                           dtype, num_splits, out, workspace, workspace_bytes, options, nullptr,
+                                           error_word, stream);
+}
+
+extern "C" pa_status pa_paged_attention_decode_strided(const void* q, const void* k_cache, const void* v_cache,
+                                                       const int32_t* block_tables, const int32_t* context_lens,
+                                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                                       int head_dim, int block_size, int num_blocks,
+                                                       int max_blocks_per_seq, float scale, pa_dtype dtype,
+                                                       int num_splits, void* out, void* workspace,
+                                                       size_t workspace_bytes, const pa_attn_options* options,
+                                                       const pa_row_strides* strides, int32_t* error_word,
+                                                       void* stream) {
   if (num_seqs < 0 || num_splits < 0 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0) return PA_OK;
   if (!context_lens) return PA_ERR_INVALID_ARGUMENT;
   pa_status st = validate_common(q, k_cache, v_cache, block_tables, out, num_q_heads, num_kv_heads, head_dim,
                                  block_size, num_blocks, max_blocks_per_seq, scale, dtype);
   if (st != PA_OK) return st;
+  long long q_stride = 0, out_stride = 0;
+  if (!resolve_strides(strides, num_q_heads, head_dim, dtype, &q_stride, &out_stride)) return PA_ERR_INVALID_ARGUMENT;
   if ((long long)num_seqs * num_kv_heads * kMaxSplits > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
   DecodeParams p{};
   p.q = q;
@@ -376,6 +431,8 @@ extern "C" pa_status pa_paged_attention_decode_ex(const void* q, const void* k_c
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.max_blocks = max_blocks_per_seq;
+  p.q_stride = q_stride;
+  p.out_stride = out_stride;
   const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
   p.scale_log2 = sc * kLog2e;
   st = apply_options(options, sc, p);
@@ -423,12 +480,29 @@ extern "C" pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_c
                                                   int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
                                                   void* out, const pa_attn_options* options, void* workspace,
                                                   size_t workspace_bytes, int32_t* error_word, void* stream) {
+  return pa_paged_attention_varlen_strided(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, num_reqs,
+                                           num_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim,
+                                           block_size, num_blocks, max_blocks_per_seq, causal, scale, dtype, out,
+                                           options, nullptr, workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" pa_status pa_paged_attention_varlen_strided(const void* q, const void* k_cache, const void* v_cache,
+                                                       const int32_t* query_start_loc, const int32_t* seq_lens,
+                                                       const int32_t* block_tables, int num_reqs, int num_tokens,
+                                                       int max_query_len, int num_q_heads, int num_kv_heads,
+                                                       int head_dim, int block_size, int num_blocks,
+                                                       int max_blocks_per_seq, int causal, float scale,
+                                                       pa_dtype dtype, void* out, const pa_attn_options* options,
+                                                       const pa_row_strides* strides, void* workspace,
+                                                       size_t workspace_bytes, int32_t* error_word, void* stream) {
   if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_reqs == 0 || num_tokens == 0) return PA_OK;
   if (!query_start_loc || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
   pa_status st = validate_common(q, k_cache, v_cache, block_tables, out, num_q_heads, num_kv_heads, head_dim,
                                  block_size, num_blocks, max_blocks_per_seq, scale, dtype);
   if (st != PA_OK) return st;
+  long long q_stride = 0, out_stride = 0;
+  if (!resolve_strides(strides, num_q_heads, head_dim, dtype, &q_stride, &out_stride)) return PA_ERR_INVALID_ARGUMENT;
   if ((long long)num_tokens * num_kv_heads > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
   const int G = num_q_heads / num_kv_heads;
   const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
@@ -460,6 +534,8 @@ extern "C" pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_c
       dp.block_size = block_size;
       dp.num_blocks = num_blocks;
       dp.max_blocks = max_blocks_per_seq;
+      dp.q_stride = q_stride;
+      dp.out_stride = out_stride;
       dp.scale_log2 = sc * kLog2e;
       st = apply_options(options, sc, dp);
       if (st != PA_OK) return st;
@@ -482,6 +558,7 @@ extern "C" pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_c
     vp.num_blocks = num_blocks;
     vp.max_blocks = max_blocks_per_seq;
     vp.max_query_len = max_query_len;
+    vp.out_stride = out_stride;
     const int tokens_per_tile = 128 / G;
     vp.q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
     vp.causal = causal ? 1 : 0;
@@ -489,7 +566,7 @@ extern "C" pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_c
     st = apply_options(options, sc, vp);
     if (st != PA_OK) return st;
     CUtensorMap qmap, kmap, vmap;
-    if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile) ||
+    if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile, q_stride) ||
         !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks,
                           block_size < 128 ? block_size : 128) ||
         !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks,
@@ -519,6 +596,8 @@ extern "C" pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_c
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.max_blocks = max_blocks_per_seq;
+  p.q_stride = q_stride;
+  p.out_stride = out_stride;
   p.scale_log2 = sc * kLog2e;
   st = apply_options(options, sc, p);
   if (st != PA_OK) return st;
@@ -775,7 +854,7 @@ extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const
   vp.ws_ml = ws_ml;
   vp.slot_count = slots;
   CUtensorMap qmap, kmap, vmap;
-  if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_seqs, G, 128 / G) ||
+  if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_seqs, G, 128 / G, (long long)num_q_heads * head_dim) ||
       !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, block_size) ||
       !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, block_size))
     return PA_ERR_CUDA;

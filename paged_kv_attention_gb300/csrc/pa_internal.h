@@ -58,11 +58,16 @@ struct DecodeParams {
   int force_partial;
   int slot_offset;
   int slot_count;
+  // elements from one query row (a sequence or token) of q / out to the next; 0 = dense (Hq * D)
+  long long q_stride;
+  long long out_stride;
 };
 
+// key_stride / value_stride: bytes from one token's row to the next (multiples of 16)
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                      const int32_t* slot_mapping, int num_tokens, int row_bytes,
-                                     long long num_slots, int32_t* err, cudaStream_t stream);
+                                     long long key_stride, long long value_stride, long long num_slots,
+                                     int32_t* err, cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t stream);
 
@@ -118,6 +123,9 @@ struct VarlenParams {
   float* ws_acc;
   float* ws_ml;
   int slot_count;
+  // elements from one token's output row to the next; 0 = dense (Hq * D). The query row stride
+  // is carried by the query tensor map.
+  long long out_stride;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
 int varlen_tc_tokens_per_cta(int group);

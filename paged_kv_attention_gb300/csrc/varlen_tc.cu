@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows = min(2 * TOK, q_len - tok0) * G;
     for (int i = tid; i < rows * (kD / 8); i += blockDim.x) {
       const int row = i / (kD / 8), c = i % (kD / 8);
-      const size_t o = ((size_t)(q_start + tok0 + row / G) * p.num_q_heads + kvh * G + row % G) * kD + c * 8;
+      const size_t o = (size_t)(q_start + tok0 + row / G) * p.out_stride + (size_t)(kvh * G + row % G) * kD + c * 8;
       *reinterpret_cast<uint4*>(out + o) = make_uint4(0, 0, 0, 0);
     }
     return;
@@ -628,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (n_mine > 0) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                           ((size_t)(q_start + tok) * p.num_q_heads + kvh * G + row % G) * kD;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)(q_start + tok) * p.out_stride +
+                           (size_t)(kvh * G + row % G) * kD;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t ov[32];
@@ -684,8 +684,10 @@ bool varlen_tc_supported(int head_dim, int group, int block_size) {
 
 int varlen_tc_tokens_per_cta(int group) { return 2 * (kBM / group); }
 
-cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+cudaError_t launch_varlen_tc(const VarlenParams& p_in, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {
+  VarlenParams p = p_in;
+  if (p.out_stride == 0) p.out_stride = (long long)p.num_q_heads * kD;  // dense rows
   // the shared-memory opt-in is per device and kernel; setting it twice is harmless
   static std::atomic<bool> attr_done[64][2] = {};
   int dev = 0;

@@ -161,6 +161,40 @@ def test_varlen_and_cache_write_refuse_bad_arguments(lib):
         _lib.PA_ERR_UNSUPPORTED                                       # 8-byte rows
 
 
+# a layout that passes the stride checks stops at the next one: the workspace (with a GPU) or the
+# device query (without one); neither launches anything
+PASSED = (_lib.PA_ERR_WORKSPACE_TOO_SMALL, _lib.PA_ERR_CUDA)
+
+
+@pytest.mark.parametrize("q_stride,out_stride,status", [
+    (0, 0, PASSED),
+    (8 * 128 + 64, 0, PASSED),
+    (8 * 128 - 8, 0, _lib.PA_ERR_INVALID_ARGUMENT),   # rows would overlap
+    (0, 8 * 128 + 4, _lib.PA_ERR_INVALID_ARGUMENT),   # 8-byte rows: not a whole 16-byte unit
+    (-8, 0, _lib.PA_ERR_INVALID_ARGUMENT),
+])
+def test_strided_calls_check_row_strides_before_launch(lib, q_stride, out_stride, status):
+    # two sequences and 4 splits: the dense layout reaches the workspace check (no launch)
+    args = _decode_args(S=2, splits=4)
+    st = _lib.RowStrides(q_stride, out_stride)
+    got = lib.pa_paged_attention_decode_strided(*args[:18], None, ctypes.byref(st), None, None)
+    assert got in status if isinstance(status, tuple) else got == status
+    bf16 = _lib.PA_DTYPE_BF16
+    # pa_paged_attention_varlen_strided(q,k,v,qsl,lens,tables, R,N,maxq, Hq,Hkv,D,bs,nb,mb, causal,scale,dtype,
+    #                                   out,options,strides,ws,ws_bytes,err,stream)
+    if status == _lib.PA_ERR_INVALID_ARGUMENT:
+        v = [16, 16, 16, 16, 16, 16, 2, 5, 4, 8, 2, 128, 16, 4, 16, 1, 0.0, bf16, 16, None, ctypes.byref(st),
+             None, 0, None, None]
+        assert lib.pa_paged_attention_varlen_strided(*v) == status
+    # key/value row strides of the cache write: Hkv * D = 256 elements dense
+    assert lib.pa_reshape_and_cache_strided(16, 16, 255, 0, 16, 16, 16, 3, 2, 128, 16, 4, bf16, None, None) == \
+        _lib.PA_ERR_INVALID_ARGUMENT
+    assert lib.pa_reshape_and_cache_strided(16, 16, 0, 260, 16, 16, 16, 3, 2, 128, 16, 4, bf16, None, None) == \
+        _lib.PA_ERR_INVALID_ARGUMENT
+    assert lib.pa_reshape_and_cache_strided(16, 16, 264, 0, 16, 16, 16, 0, 2, 128, 16, 4, bf16, None, None) == \
+        _lib.PA_OK                                                    # no tokens: nothing launched
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
