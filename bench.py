@@ -401,9 +401,10 @@ def decode_leg(args, world, rank, dev):
                 launches=args.steps * (2 + (1 if splits > 1 else 0)))
 
 
-def decode_int8_leg(args, dev):
-    """The same 64x4096 decode over an int8 cache (codes + one fp32 scale per (slot, KV head)),
-    quantised by the library's own write; the decode call replayed as a CUDA graph."""
+def decode_int8_leg(args, dev, code_dtype=torch.int8):
+    """The same 64x4096 decode over an 8-bit cache (int8 or fp8 E4M3 codes + one fp32 scale per
+    (slot, KV head)), quantised by the library's own write; the decode call replayed as a CUDA
+    graph."""
     import paged_kv_attention_gb300 as pa
     import workloads
     case = workloads.NAMED[DECODE_WORKLOAD]()
@@ -413,8 +414,8 @@ def decode_int8_leg(args, dev):
                                      dtype=torch.bfloat16)
     S, Hq, Hkv, D, bs = case.num_reqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
     shape = (case.num_blocks, bs, Hkv, D)
-    kc = torch.empty(shape, dtype=torch.int8, device=dev)
-    vc = torch.empty(shape, dtype=torch.int8, device=dev)
+    kc = torch.empty(shape, dtype=code_dtype, device=dev)
+    vc = torch.empty(shape, dtype=code_dtype, device=dev)
     ks = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     vs = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     pa.reshape_and_cache_quant(case.key.to(dev), case.value.to(dev), kc, vc, ks, vs, case.slot_mapping.to(dev))
@@ -576,7 +577,7 @@ def main():
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the decode step eagerly, not as CUDA graphs")
-    ap.add_argument("--no-int8", action="store_true", help="skip the int8-cache decode leg")
+    ap.add_argument("--no-int8", action="store_true", help="skip the 8-bit-cache decode legs (int8, fp8 E4M3)")
     ap.add_argument("--no-cascade", action="store_true", help="skip the shared-prefix (cascade) decode leg")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -610,6 +611,7 @@ def main():
         d = None if args.only == "prefill" else decode_leg(args, world, rank, dev)
         p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps)
         q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
+        f8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev, torch.float8_e4m3fn)
         cz = None if (args.no_cascade or args.only != "all") else cascade_leg(args, dev)
     clk = clocks.summary()
     if d is None:
@@ -670,6 +672,12 @@ def main():
             "value": round(q8["gbs"], 2), "unit": "GB/s", "call_ms": round(q8["ms"], 5),
             "algorithmic_bytes_per_launch": q8["bytes"], "frac_of_hbm_peak": round(q8["gbs"] / hbm, 4),
             "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3), "traffic": traffic.get("decode_int8_kernel")}
+    if f8 is not None:
+        line["decode_fp8"] = {
+            "workload": "decode_64x4096_fp8_e4m3 (same queries and tokens, E4M3 codes + fp32 scales)",
+            "value": round(f8["gbs"], 2), "unit": "GB/s", "call_ms": round(f8["ms"], 5),
+            "algorithmic_bytes_per_launch": f8["bytes"], "frac_of_hbm_peak": round(f8["gbs"] / hbm, 4),
+            "speedup_vs_bf16_call": round(d["call_ms"] / f8["ms"], 3)}
     if cz is not None:
         cms = cz["cascade_ms"]
         line["cascade"] = {

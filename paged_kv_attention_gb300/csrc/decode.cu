@@ -23,7 +23,6 @@
 #include <atomic>
 
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -256,8 +255,9 @@ __device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w, uint32_t sel) {
   } else {
     // the same two bytes, packed into the low half-word, through the E4M3 -> f16x2 conversion
     const uint32_t pair = __byte_perm(w, 0u, (sel & 0xfu) | ((sel & 0xf00u) >> 4));
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)pair));
+    return h;
   }
 }
 // selectors (result bytes 0 and 2 carry the codes; bytes 1 and 3 take 0x64 from the constant)
@@ -804,6 +804,19 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   }
   const int D = p.head_dim;
   const size_t base = (size_t)unit * S * p.num_q_heads + h;  // slot of split s: base + s * Hq
+  // Sixteen partials' loads per batch are issued before any of them is used, so their latencies
+  // overlap; the first batch is requested before the weights, so it overlaps the (m, l) loads too.
+  constexpr int kBatch = 8;
+  auto load_batch = [&](int d0, int s0, float4 (&v)[kBatch]) {
+    const int d = d0 + lane * 4;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      v[k] = (d < D && s0 + k < S)
+                 ? *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)(s0 + k) * p.num_q_heads) * D + d)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  float4 first[kBatch];
+  load_batch(0, 0, first);
   const float m_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2] : -INFINITY;
   const float l_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2 + 1] : 0.f;
   float M = m_s;
@@ -821,20 +834,19 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   OutT* out = reinterpret_cast<OutT*>(p.out) + (size_t)q_row * p.out_stride + (size_t)h * D;
   // every lane runs every iteration (the weight shuffles need the whole warp); lanes past
-  // the head dim only skip their loads and stores. Sixteen partials' loads are issued before
-  // any of them is used, so their latencies overlap.
-  constexpr int kBatch = 16;
+  // the head dim only skip their loads and stores
   for (int d0 = 0; d0 < D; d0 += 128) {
     const int d = d0 + lane * 4;
     const bool active = d < D;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < S; s0 += kBatch) {
       float4 v[kBatch];
+      if (d0 == 0 && s0 == 0) {
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-        v[k] = (active && s0 + k < S)
-                   ? *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)(s0 + k) * p.num_q_heads) * D + d)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < kBatch; ++k) v[k] = first[k];
+      } else {
+        load_batch(d0, s0, v);
+      }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const float ws = __shfl_sync(0xffffffffu, w, (s0 + k) & 31);  // w = 0 on lanes >= S
