@@ -562,6 +562,92 @@ def prefill_leg(args, dev, steps):
                 launches=2 * steps)
 
 
+def configs_leg(args, dev, peaks):
+    """The other workloads of the hot path (the parity configurations): the fp32 latency case,
+    the ragged bf16 decode, the head_dim-256 decode and the mixed varlen batch. Each call is
+    captured in a CUDA graph and replayed; before every timed call 256 MB are rewritten and
+    re-read so that no input stays in L2 (the fp32 case, whose 0.2 MB live in L2 between steps
+    of a real decode loop, is also timed warm); CUDA events on the call's stream; median and
+    minimum of `n` calls. The two small decodes are also launched eagerly."""
+    import paged_kv_attention_gb300 as pa
+    import workloads
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rd = torch.zeros(64 << 20, device=dev)
+
+    def timed(fn, n=50, graph=True, cold=True):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        run = fn
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            for _ in range(3):
+                g.replay()
+            run = g.replay
+        events = []
+        for _ in range(n):
+            if cold:
+                flush.fill_(1)
+                rd.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            events.append((e0, e1))
+        torch.cuda.synchronize()
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in events)
+        return statistics.median(us), us[0]
+
+    hbm, tf = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    res = {}
+    for name in ("decode_1seq_fp32", "decode_ragged32_bf16", "decode_64x4096_bf16_d256"):
+        case = workloads.NAMED[name]()
+        kc, vc = (t.to(dev) for t in case.empty_pools())
+        pa.reshape_and_cache(case.key.to(dev), case.value.to(dev), kc, vc, case.slot_mapping.to(dev))
+        q, t, lens = case.q.to(dev), case.block_tables.to(dev), case.seq_lens.to(dev)
+        o = torch.empty_like(q)
+        S, Hq, Hkv, D, bs = case.num_reqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
+        splits = pa.decode_auto_splits(S, Hq, Hkv, D, bs, t.shape[1], case.dtype)
+        ws = torch.empty(max(pa.decode_workspace_bytes(S, Hq, D, t.shape[1], bs, splits), 16), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            pa.paged_attention_decode(q, kc, vc, t, lens, case.scale, out=o, workspace=ws)
+
+        med, mn = timed(call)
+        elt = 4 if case.dtype == torch.float32 else 2
+        kv = sum(int(x) for x in case.seq_lens) * Hkv * D * elt * 2
+        entry = {"us_median": round(med, 2), "us_min": round(mn, 2), "splits": splits, "kv_bytes": kv,
+                 "GBps": round(kv / med / 1e3, 1), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
+        if name != "decode_64x4096_bf16_d256":
+            emed, emn = timed(call, graph=False)
+            entry["eager_us_median"], entry["eager_us_min"] = round(emed, 2), round(emn, 2)
+        if name == "decode_1seq_fp32":
+            wmed, wmn = timed(call, cold=False)
+            entry["warm_us_median"], entry["warm_us_min"] = round(wmed, 2), round(wmn, 2)
+        res[name] = entry
+    case = workloads.NAMED["varlen_mixed_bf16"]()
+    kc, vc = (t.to(dev) for t in case.empty_pools())
+    pa.reshape_and_cache(case.key.to(dev), case.value.to(dev), kc, vc, case.slot_mapping.to(dev))
+    q = case.q.to(dev)
+    o = torch.empty_like(q)
+    a = (kc, vc, case.query_start_loc.to(dev), case.seq_lens.to(dev), case.block_tables.to(dev), case.max_query_len,
+         True, case.scale)
+    med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o))
+    qls = (case.query_start_loc[1:] - case.query_start_loc[:-1]).tolist()
+    sls = case.seq_lens.tolist()
+    pairs = sum(sum(min(L - ql + i + 1, L) for i in range(ql)) for ql, L in zip(qls, sls))
+    flops = 4 * case.head_dim * case.num_q_heads * pairs
+    kv = sum(sls) * case.num_kv_heads * case.head_dim * 2 * 2
+    res["varlen_mixed_bf16"] = {
+        "us_median": round(med, 2), "us_min": round(mn, 2), "causal_flops": flops, "kv_bytes": kv,
+        "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
+        "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,8 +657,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "int8", "cascade"], default="all",
-                    help="run one leg only (profiling runs)")
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "int8", "cascade", "configs"], default="all",
+                    help="run one leg only (profiling runs); 'configs' times the parity configurations")
     ap.add_argument("--decode-seqs", type=int, default=64, help="sequences of 4096 tokens in the decode leg")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
     ap.add_argument("--no-e2e", action="store_true")
@@ -593,6 +679,12 @@ def main():
     peaks, peak_src = load_peaks()
     traffic = load_traffic()
 
+    if args.only == "configs":
+        r = configs_leg(args, dev, peaks)
+        if rank == 0:
+            print(json.dumps({"configs": r, "peak_source": peak_src, "l2": "256 MB rewritten and re-read before "
+                              "every timed call"}), flush=True)
+        return
     if args.only == "cascade":
         c = cascade_leg(args, dev)
         if rank == 0:

@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
     for (int g = 0; g < GP; ++g) s[g] = 0.f;
     if (valid && row >= 0) {
       const float4* kr = reinterpret_cast<const float4*>(kc + (size_t)row * row_elems + (size_t)kvh * D);
-#pragma unroll 4
+#pragma unroll 8
       for (int d4 = 0; d4 < D / 4; ++d4) {
         const float4 k4 = __ldg(kr + d4);
 #pragma unroll
@@ -748,19 +748,28 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
       my_p[g * 32 + lane] = pr;
     }
     __syncwarp();
+    // value rows in batches whose loads are all issued before the first is used (one memory
+    // latency per batch, not per key); a row past the end or outside the pool reads as zeros
+    // and its probability is 0
     const int nk = min(32, k_end - kb);
-    for (int j = 0; j < nk; ++j) {
-      const long long vr = my_vrow[j];
-      if (vr < 0) continue;  // a page outside the pool contributes nothing
-      const float* vrp = vc + (size_t)vr * row_elems + (size_t)kvh * D;
-      float vv[DL];
+    constexpr int kVB = DL >= 8 ? 4 : 8;
+    for (int j0 = 0; j0 < nk; j0 += kVB) {
+      float vv[kVB][DL];
 #pragma unroll
-      for (int c = 0; c < DL; ++c) vv[c] = __ldg(vrp + lane + 32 * c);
+      for (int b = 0; b < kVB; ++b) {
+        const long long vr = j0 + b < nk ? my_vrow[j0 + b] : -1;
+        const float* vrp = vc + (size_t)(vr < 0 ? 0 : vr) * row_elems + (size_t)kvh * D;
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float pj = my_p[g * 32 + j];
+        for (int c = 0; c < DL; ++c) vv[b][c] = vr >= 0 ? __ldg(vrp + lane + 32 * c) : 0.f;
+      }
 #pragma unroll
-        for (int c = 0; c < DL; ++c) acc[g][c] = fmaf(pj, vv[c], acc[g][c]);
+      for (int b = 0; b < kVB; ++b) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float pj = my_p[g * 32 + j0 + b];
+#pragma unroll
+          for (int c = 0; c < DL; ++c) acc[g][c] = fmaf(pj, vv[b][c], acc[g][c]);
+        }
       }
     }
     __syncwarp();
