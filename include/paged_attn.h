@@ -275,9 +275,11 @@ pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const
                                        void* stream);
 
 /* pa_paged_attention_varlen_ex with a workspace. The same result; with a non-NULL workspace the
- * batch's one-query (decode) requests are served by the split-KV decode (its splits keep long
- * contexts streaming at HBM speed) and every other request by the tensor-core kernel; with NULL
- * this is pa_paged_attention_varlen_ex. workspace: device memory of
+ * batch's short requests (1 to 8 queries: decodes and speculative verify blocks) are served by
+ * the split-KV decode (its splits keep long contexts streaming at HBM speed; each query sees
+ * its own causal range) and every other request by the tensor-core kernel ("TileInfer.jl -
+ * Attention kernels", Decode: GQA packing and split-KV, the verify step); with NULL this is
+ * pa_paged_attention_varlen_ex. workspace: device memory of
  * >= pa_varlen_workspace_bytes(...) bytes, 16-byte aligned, fully overwritten, not shared by
  * calls that overlap on the GPU; PA_ERR_WORKSPACE_TOO_SMALL when it is shorter. Two launches
  * (three with the decode's combine) on `stream`. */
@@ -304,8 +306,10 @@ pa_status pa_paged_attention_varlen_strided(const void* q, const void* k_cache, 
                                             const pa_row_strides* strides, void* workspace,
                                             size_t workspace_bytes, int32_t* error_word, void* stream);
 
-/* Workspace bytes pa_paged_attention_varlen_ws needs (the split partials of num_reqs one-query
- * requests at any split count; the decode bound of pa_decode_workspace_bytes). Host only. */
+/* Workspace bytes pa_paged_attention_varlen_ws needs: the split partials of num_reqs short
+ * requests (8 queries per request, at most 8 splits): num_reqs * 8 * min(8, chunks) * Hq *
+ * (D + 2) * 4 with chunks = cdiv(max_blocks_per_seq * block_size, 16); 0 when one split covers
+ * every context. Host only. */
 size_t pa_varlen_workspace_bytes(int num_reqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
                                  int block_size);
 

@@ -188,10 +188,10 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            split_decodes: bool = False) -> torch.Tensor:
     """Flattened prefill / verify / decode batch; request r's queries are the newest q_len of
     its seq_lens[r] positions, causal by position. ``window``, ``softcap`` and ``sinks`` are
-    the pa_attn_options score modifiers. With ``split_decodes`` (bf16), the batch's one-query
-    requests go to the split-KV decode (a workspace is allocated unless one is given): faster
-    for batches that are mostly decodes, slower for prefill-heavy ones (two launches in turn
-    instead of one grid)."""
+    the pa_attn_options score modifiers. With ``split_decodes`` (bf16), the batch's short
+    requests (1 to 8 queries: decodes, verify blocks) go to the split-KV decode (a workspace is
+    allocated unless one is given): faster for batches of short requests, slower for
+    prefill-heavy ones (two launches in turn instead of one grid)."""
     n, hq, d = q.shape
     nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     r = seq_lens.shape[0]

@@ -42,16 +42,20 @@ namespace {
 
 // ------------------------------------------------------------------ unit resolution
 struct Unit {
-  int len;        // keys visible to every row of the unit: positions [start, len)
-  int start;      // first visible position (> 0 only under a sliding window)
+  int len;        // keys [start, len) are loaded; the unit's last query sees all of them
+  int start;      // first position any query of the unit sees (> 0 only under a sliding window)
   int table_row;  // block table row
-  int q_row;      // row of q / out
+  int q_row;      // row of q / out of the unit's first query
+  int n_tok;      // queries of the unit (consecutive rows of q); its rows are n_tok * group
+  int first_pos;  // position of the unit's first query; query t sits at first_pos + t
   bool skip;      // not this launch's unit: write nothing
 };
 
 __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bool report) {
   Unit u;
   u.skip = false;
+  u.n_tok = 1;
+  u.first_pos = 0;
   int len;
   if (p.varlen == 0) {
     u.table_row = unit;
@@ -59,24 +63,33 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     len = p.context_lens[unit];
     u.start = 0;
   } else if (p.varlen == 2) {
-    // a varlen request served only if it has exactly one query, at its newest position: it then
-    // sees all seq_len keys, causal or not (the tensor-core kernel takes every other request)
-    const int start = p.query_start_loc[unit];
-    const int stop = p.query_start_loc[unit + 1];
-    u.table_row = unit;
-    u.q_row = start;
+    // request units: a request with 1 <= q_len <= small_max, its queries in groups of
+    // unit_tokens (group g of request r is unit r * groups_per_req + g); every other request is
+    // left to the tensor-core kernel and nothing is written for it here
+    const int r = unit / p.groups_per_req;
+    const int g = unit - r * p.groups_per_req;
+    const int start = p.query_start_loc[r];
+    const int q_len = p.query_start_loc[r + 1] - start;
+    const int tok0 = g * p.unit_tokens;
+    u.table_row = r;
     u.start = 0;
-    if (stop - start != 1 || start < 0) {
-      u.skip = true;
+    u.q_row = start + tok0;
+    if (start < 0 || q_len < 1 || q_len > p.small_max || tok0 >= q_len || start + q_len > p.num_tokens) {
+      u.skip = true;  // (a query block past the last row is flagged by the tensor-core kernel)
       len = 0;
     } else {
-      len = p.seq_lens[unit];
-      if (len < 1) {  // the query's own position is not cached: a layout error, zero row
+      u.n_tok = min(p.unit_tokens, q_len - tok0);
+      const int seq = p.seq_lens[r];
+      if (q_len > seq) {  // the queries' own positions are not all cached: a layout error, zero rows
         if (report) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
         len = 0;
-      } else if (len > p.max_blocks * p.block_size) {  // as the varlen kernels: zero row, flag
+      } else if (seq > p.max_blocks * p.block_size) {  // as the varlen kernels: zero rows, flag
         if (report) flag_error(p.err, PA_ERRBIT_LENGTH_OUT_OF_RANGE);
         len = 0;
+      } else {
+        u.first_pos = seq - q_len + tok0;  // queries are the request's newest positions
+        len = p.causal ? u.first_pos + u.n_tok : seq;
+        if (p.window > 0) u.start = max(0, u.first_pos - p.window + 1);
       }
     }
   } else {
@@ -102,6 +115,7 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     } else {
       const int pos = seq - q_len + (unit - start);  // queries are the newest positions
       len = p.causal ? pos + 1 : seq;
+      u.first_pos = pos;
       if (p.window > 0) u.start = max(0, pos - p.window + 1);
     }
   }
@@ -111,8 +125,11 @@ __device__ __forceinline__ Unit resolve_unit(const DecodeParams& p, int unit, bo
     len = len < 0 ? 0 : cap;
   }
   u.len = len;
-  // decode: the query is the newest cached position, len - 1
-  if (p.varlen != 1 && p.window > 0) u.start = max(0, len - p.window);
+  if (p.varlen == 0) {
+    // decode: the query is the newest cached position, len - 1
+    u.first_pos = len - 1;
+    if (p.window > 0) u.start = max(0, len - p.window);
+  }
   if (u.start > u.len) u.start = u.len;
   return u;
 }
@@ -132,12 +149,14 @@ __device__ __forceinline__ float score_log2(const DecodeParams& p, float s) {
 //   mo: [nw][rows][D] accumulators, ml: [nw][rows][2] (m in log2 units, l)
 template <typename OutT>
 __device__ __forceinline__ void merge_and_store(const DecodeParams& p, const float* mo, const float* ml, int nw,
-                                                int rows, int D, int unit, int q_row, int kvh, int split) {
+                                                int rows, int D, int unit, const Unit& u, int kvh, int split) {
   const int G = p.group;
-  const int h0 = kvh * G;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+  // row n of the state: query t = n / G of the unit, head kvh * G + n % G
+  for (int idx = threadIdx.x; idx < u.n_tok * G * D; idx += blockDim.x) {
     const int n = idx / D;
     const int d = idx - n * D;
+    const int t = n / G;
+    const int h = kvh * G + (n - t * G);
     float M = -INFINITY;
     for (int w = 0; w < nw; ++w) M = fmaxf(M, ml[(w * rows + n) * 2]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
@@ -148,12 +167,14 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, const flo
       O += wt * mo[(w * rows + n) * D + d];
     }
     if (p.num_splits == 1 && !p.force_partial) {
-      if (p.sinks != nullptr) O *= fold_sink(p.sinks[h0 + n], M, L);
+      if (p.sinks != nullptr) O *= fold_sink(p.sinks[h], M, L);
       const float v = (L > 0.f) ? O / L : 0.f;
       OutT* out = reinterpret_cast<OutT*>(p.out);
-      out[(size_t)q_row * p.out_stride + (size_t)(h0 + n) * D + d] = static_cast<OutT>(v);
+      out[(size_t)(u.q_row + t) * p.out_stride + (size_t)h * D + d] = static_cast<OutT>(v);
     } else {
-      const size_t slot = ((size_t)unit * p.slot_count + p.slot_offset + split) * p.num_q_heads + h0 + n;
+      // partial slot (unit, split, query t of the unit, head)
+      const size_t slot =
+          (((size_t)unit * p.slot_count + p.slot_offset + split) * p.unit_tokens + t) * p.num_q_heads + h;
       p.ws_acc[slot * D + d] = O;
       if (d == 0) {
         p.ws_ml[slot * 2] = M;
@@ -310,9 +331,12 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     prefetch_tensormap(&vmap);
   }
   if (p.varlen != 1 && warp >= C::kConsumers) {
+    // the unit's block-table row: the sequence, or (request units) the request of the group
+    const int spec_row = p.varlen == 2 ? unit / p.groups_per_req : unit;
     spec_base = split * p.chunks_per_split * kChunk / p.block_size;
-    spec_page = spec_base + lane < p.max_blocks ? __ldg(p.block_tables + (size_t)unit * p.max_blocks + spec_base + lane)
-                                                : -1;
+    spec_page = spec_base + lane < p.max_blocks
+                    ? __ldg(p.block_tables + (size_t)spec_row * p.max_blocks + spec_base + lane)
+                    : -1;
   }
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
   if (u.skip) return;  // uniform: another kernel serves this unit
@@ -397,28 +421,45 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     const int G = p.group;
     const int g4 = lane >> 2;  // groupID
     const int t4 = lane & 3;   // thread in group
-    // Q^T as the B operand: rows n (query heads of the group), k = head dim
+    // Q^T as the B operand: rows n = (query t = n / G of the unit, head n % G of the group),
+    // k = head dim
+    const int n_rows = u.n_tok * G;
     uint32_t qf[NT][C::kMT][2];
     {
-      const __nv_bfloat16* qb =
-          reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)u.q_row * p.q_stride + (size_t)kvh * G * D;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g4;
-        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + (size_t)n * D);
+        const bool rv = n < n_rows;
+        const int t = rv ? n / G : 0;
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(
+            reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)(u.q_row + t) * p.q_stride +
+            (size_t)(kvh * G + (rv ? n - t * G : 0)) * D);
 #pragma unroll
         for (int kk = 0; kk < C::kMT; ++kk) {
           if constexpr (QK == 0) {
-            qf[nt][kk][0] = (n < G) ? __ldg(qr + (kk * 16 + 2 * t4) / 2) : 0u;
-            qf[nt][kk][1] = (n < G) ? __ldg(qr + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
+            qf[nt][kk][0] = rv ? __ldg(qr + (kk * 16 + 2 * t4) / 2) : 0u;
+            qf[nt][kk][1] = rv ? __ldg(qr + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
           } else {
             // the codes' k-slot order (dims 4t..4t+3 of each 16-dim step), converted to fp16
-            qf[nt][kk][0] = (n < G) ? bf16x2_to_f16x2(__ldg(qr + (kk * 16 + 4 * t4) / 2)) : 0u;
-            qf[nt][kk][1] = (n < G) ? bf16x2_to_f16x2(__ldg(qr + (kk * 16 + 4 * t4 + 2) / 2)) : 0u;
+            qf[nt][kk][0] = rv ? bf16x2_to_f16x2(__ldg(qr + (kk * 16 + 4 * t4) / 2)) : 0u;
+            qf[nt][kk][1] = rv ? bf16x2_to_f16x2(__ldg(qr + (kk * 16 + 4 * t4 + 2) / 2)) : 0u;
           }
         }
       }
     }
+    // the keys each of this thread's score rows (2 t4 and 2 t4 + 1 of every 8) may see: query t
+    // of the unit sees positions [first_pos + t - window + 1, first_pos + t] when causal (all
+    // len when not); a one-query unit's rows all see [start, len)
+    int key_hi[NT][2], key_lo[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int n = nt * 8 + 2 * t4 + j;
+        const int t = n < n_rows ? n / G : u.n_tok - 1;
+        key_hi[nt][j] = p.causal ? u.len - (u.n_tok - 1 - t) : u.len;
+        key_lo[nt][j] = p.window > 0 ? u.first_pos + t - p.window + 1 : 0;
+      }
     float o[NT][C::kMT][4];
     float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -446,7 +487,6 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
       uint8_t* vt = kt + C::kTileBytes;
       const int key0 = (c_begin + i) * kChunk;
       const int nvalid = min(kChunk, u.len - key0);
-      const int nlow = u.start - key0;  // keys below this index of the chunk are outside the window
       float ks_a = 1.f, ks_b = 1.f, vs_a = 1.f, vs_b = 1.f;
       // 8-bit caches: the chunk's codes go to registers (per thread 16 bytes of K and of V per
       // 128 head dims) and the stage is released before any arithmetic; at D 256 the value codes
@@ -544,8 +584,13 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         } else {
           x0 = s[nt][0] * sl2, x1 = s[nt][1] * sl2, x2 = s[nt][2] * sl2, x3 = s[nt][3] * sl2;
         }
-        if (g4 >= nvalid || g4 < nlow) x0 = x1 = -INFINITY;
-        if (g4 + 8 >= nvalid || g4 + 8 < nlow) x2 = x3 = -INFINITY;
+        {
+          const int ka = key0 + g4, kb = ka + 8;  // positions of this thread's two keys
+          if (ka >= key_hi[nt][0] || ka < key_lo[nt][0]) x0 = -INFINITY;
+          if (ka >= key_hi[nt][1] || ka < key_lo[nt][1]) x1 = -INFINITY;
+          if (kb >= key_hi[nt][0] || kb < key_lo[nt][0]) x2 = -INFINITY;
+          if (kb >= key_hi[nt][1] || kb < key_lo[nt][1]) x3 = -INFINITY;
+        }
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -650,7 +695,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
       if (i < s_issued[i % C::kProducers]) (void)mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1);
   }
   __syncthreads();
-  merge_and_store<__nv_bfloat16>(p, merge_o, merge_ml, C::kConsumers, ROWS, D, unit, u.q_row, kvh, split);
+  merge_and_store<__nv_bfloat16>(p, merge_o, merge_ml, C::kConsumers, ROWS, D, unit, u, kvh, split);
 }
 
 // ------------------------------------------------------------------ fp32 CUDA-core decode
@@ -786,7 +831,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const __grid_constant__
     for (int c = 0; c < DL; ++c) merge_o[(warp * GP + g) * D + lane + 32 * c] = acc[g][c];
   }
   __syncthreads();
-  merge_and_store<float>(p, merge_o, merge_ml, C::kWarps, GP, D, unit, u.q_row, kvh, split);
+  merge_and_store<float>(p, merge_o, merge_ml, C::kWarps, GP, D, unit, u, kvh, split);
 }
 
 // ------------------------------------------------------------------ combine
@@ -798,21 +843,29 @@ template <typename OutT>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeParams p) {
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (gw >= p.num_units * p.num_q_heads) return;
+  const int T = p.unit_tokens;  // queries per unit
+  if (gw >= p.num_units * T * p.num_q_heads) return;
   // launched as a programmatic dependent of the split kernel: wait for that grid to complete
   // and its partials to be visible (a no-op for an ordinary launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int unit = gw / p.num_q_heads;
-  const int h = gw - unit * p.num_q_heads;
+  const int unit = gw / (T * p.num_q_heads);
+  const int rem = gw - unit * T * p.num_q_heads;
+  const int t = rem / p.num_q_heads;  // query t of the unit
+  const int h = rem - t * p.num_q_heads;
   const int S = p.num_splits;
-  // the unit's output row (request units: only one-query requests were served, at their query)
+  // the row's output row (request units: only the queries the split kernel served)
   int q_row = unit;
   if (p.varlen == 2) {
-    q_row = p.query_start_loc[unit];
-    if (p.query_start_loc[unit + 1] - q_row != 1 || q_row < 0) return;
+    const int r = unit / p.groups_per_req;
+    const int tok = (unit - r * p.groups_per_req) * T + t;
+    const int start = p.query_start_loc[r];
+    const int q_len = p.query_start_loc[r + 1] - start;
+    if (start < 0 || q_len < 1 || q_len > p.small_max || tok >= q_len || start + q_len > p.num_tokens) return;
+    q_row = start + tok;
   }
   const int D = p.head_dim;
-  const size_t base = (size_t)unit * S * p.num_q_heads + h;  // slot of split s: base + s * Hq
+  const size_t sstride = (size_t)T * p.num_q_heads;       // slot of split s: base + s * sstride
+  const size_t base = (size_t)unit * S * sstride + (size_t)t * p.num_q_heads + h;
   // Sixteen partials' loads per batch are issued before any of them is used, so their latencies
   // overlap; the first batch is requested before the weights, so it overlaps the (m, l) loads too.
   constexpr int kBatch = 8;
@@ -821,13 +874,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
       v[k] = (d < D && s0 + k < S)
-                 ? *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)(s0 + k) * p.num_q_heads) * D + d)
+                 ? *reinterpret_cast<const float4*>(p.ws_acc + (base + (size_t)(s0 + k) * sstride) * D + d)
                  : make_float4(0.f, 0.f, 0.f, 0.f);
   };
   float4 first[kBatch];
   load_batch(0, 0, first);
-  const float m_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2] : -INFINITY;
-  const float l_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * p.num_q_heads) * 2 + 1] : 0.f;
+  const float m_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * sstride) * 2] : -INFINITY;
+  const float l_s = (lane < S) ? p.ws_ml[(base + (size_t)lane * sstride) * 2 + 1] : 0.f;
   float M = m_s;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -936,18 +989,22 @@ int pad_group(int g) {
   return gp;
 }
 
-// q / out row strides default to dense rows
+// q / out row strides default to dense rows; units default to one query
 DecodeParams with_row_strides(const DecodeParams& in) {
   DecodeParams p = in;
   if (p.q_stride == 0) p.q_stride = (long long)p.num_q_heads * p.head_dim;
   if (p.out_stride == 0) p.out_stride = (long long)p.num_q_heads * p.head_dim;
+  if (p.unit_tokens < 1) p.unit_tokens = 1;
+  if (p.groups_per_req < 1) p.groups_per_req = 1;
   return p;
 }
 
 }  // namespace
 
-#define PA_TC_NT(D, QK) \
-  (p.group > 8 ? launch_tc_impl<D, 2, QK>(p, kmap, vmap, stream) : launch_tc_impl<D, 1, QK>(p, kmap, vmap, stream))
+// one n-tile of 8 rows, or two for up to 16 rows (rows = unit queries x group)
+#define PA_TC_NT(D, QK)                                                                 \
+  (p.unit_tokens * p.group > 8 ? launch_tc_impl<D, 2, QK>(p, kmap, vmap, stream)        \
+                               : launch_tc_impl<D, 1, QK>(p, kmap, vmap, stream))
 
 cudaError_t launch_decode_bf16(const DecodeParams& p_in, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream) {
@@ -1021,7 +1078,7 @@ int decode_f32_ctas_per_sm(int head_dim, int group) {
 
 cudaError_t launch_combine(const DecodeParams& p_in, pa_dtype dtype, cudaStream_t stream) {
   const DecodeParams p = with_row_strides(p_in);
-  const long long warps = (long long)p.num_units * p.num_q_heads;
+  const long long warps = (long long)p.num_units * p.unit_tokens * p.num_q_heads;
   const unsigned blocks = (unsigned)((warps + 3) / 4);
   // programmatic dependent launch: the combine's CTAs launch while the split kernel's last CTAs
   // merge and store, and wait in-kernel for its completion

@@ -246,11 +246,19 @@ pa_status validate_common(const void* q, const void* k_cache, const void* v_cach
 }
 
 // Preferred shortest split, in 16-token chunks (measured on GB300 at 64 x 4096: bf16 calls ran
-// 171 us at the wave-filling 7 splits and 167 us at 3-4; int8-code calls, limited by their
-// consumers rather than HBM, 160 us at 7 splits and 112 us at 1; fp8-code calls 169 us at 7,
-// 148 us at 1).
+// 171 us at the wave-filling 7 splits and 167 us at 3-4; 8-bit-code calls, limited by their
+// consumers rather than HBM, 160 us at 7 splits and 112-113 us at 1).
 constexpr int kMinChunksPerSplitBf16 = 64;
 constexpr int kMinChunksPerSplitCodes = 256;
+
+// Varlen requests of at most this many queries (decodes, speculative verify blocks) go to the
+// split-KV decode when the caller gives pa_paged_attention_varlen_ws a workspace; they run as
+// units of up to 8 query rows (unit_tokens queries x group: one MMA n-tile) with at most 8
+// splits. (Units of 16 rows, two n-tiles, read a verify block's keys fewer times but measured
+// slower: 48 vs 46 us for 8 verify blocks of 5 queries, 103 vs 87 us for 48 decodes.)
+constexpr int kShortRequestQueries = 8;
+constexpr int kShortRequestMaxSplits = 8;
+int short_unit_tokens(int G) { return std::min(kShortRequestQueries, std::max(1, 8 / G)); }
 
 int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long max_chunks, pa_dtype dtype,
                 int quant = 0) {
@@ -285,8 +293,11 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   if (!device_info(&info)) return PA_ERR_CUDA;
   const int D = p.head_dim;
   const long long max_chunks = cdivll((long long)p.max_blocks * p.block_size, kChunk);
+  const int T = std::max(1, p.unit_tokens);  // queries per unit; the kernel's rows are T * group
   int splits = requested_splits;
-  if (splits <= 0) splits = auto_splits(info, p.num_units, p.num_kv_heads, D, p.group, max_chunks, dtype, p.quant);
+  if (splits <= 0)
+    splits = auto_splits(info, p.num_units, p.num_kv_heads, D, p.group * T, max_chunks, dtype, p.quant);
+  if (p.varlen == 2) splits = std::min(splits, kShortRequestMaxSplits);
   splits = (int)std::min<long long>(splits, max_chunks);
   const int per = (int)cdivll(max_chunks, splits);
   splits = (int)cdivll(max_chunks, per);
@@ -296,11 +307,12 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   p.slot_offset = 0;
   p.force_partial = 0;
   if (splits > 1) {
-    const size_t need = (size_t)p.num_units * splits * p.num_q_heads * ((size_t)D + 2) * 4;
+    const size_t slots = (size_t)p.num_units * splits * T * p.num_q_heads;
+    const size_t need = slots * ((size_t)D + 2) * 4;
     if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(workspace)) return PA_ERR_INVALID_ARGUMENT;
     p.ws_acc = static_cast<float*>(workspace);
-    p.ws_ml = p.ws_acc + (size_t)p.num_units * splits * p.num_q_heads * D;
+    p.ws_ml = p.ws_acc + slots * D;
   }
   cudaError_t e;
   if (dtype == PA_DTYPE_BF16 || p.quant != 0) {
@@ -455,7 +467,13 @@ extern "C" pa_status pa_paged_attention_varlen(const void* q, const void* k_cach
 
 extern "C" size_t pa_varlen_workspace_bytes(int num_reqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
                                             int block_size) {
-  return pa_decode_workspace_bytes(num_reqs, num_q_heads, head_dim, max_blocks_per_seq, block_size, 0);
+  // units x queries per unit = num_reqs x kShortRequestQueries for every group size (the unit
+  // sizes divide it), at most kShortRequestMaxSplits splits
+  if (num_reqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0) return 0;
+  const long long max_chunks = cdivll((long long)max_blocks_per_seq * block_size, kChunk);
+  const long long splits = std::min<long long>(kShortRequestMaxSplits, max_chunks);
+  if (splits <= 1) return 0;
+  return (size_t)((long long)num_reqs * kShortRequestQueries * splits * num_q_heads * ((long long)head_dim + 2) * 4);
 }
 
 extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -509,9 +527,10 @@ extern "C" pa_status pa_paged_attention_varlen_strided(const void* q, const void
   cudaStream_t s = as_stream(stream);
 
   if (dtype == PA_DTYPE_BF16 && varlen_tc_supported(head_dim, G, block_size) && max_query_len > 0) {
-    // With a workspace, the one-query (decode) requests of the batch go to the split-KV decode,
-    // whose splits keep long contexts streaming at HBM speed; a 128-row tensor-core tile would
-    // carry G valid rows for them. The tensor-core kernel takes every other request.
+    // With a workspace, the short requests of the batch (decodes, verify blocks of up to
+    // kShortRequestQueries queries) go to the split-KV decode, whose splits keep long contexts
+    // streaming at HBM speed; a 128-row tensor-core tile would carry only their few rows, in one
+    // CTA per request and KV head. The tensor-core kernel takes every other request.
     const bool split_decodes = workspace != nullptr;
     if (split_decodes) {
       DecodeParams dp{};
@@ -526,7 +545,13 @@ extern "C" pa_status pa_paged_attention_varlen_strided(const void* q, const void
       dp.varlen = 2;
       dp.causal = causal ? 1 : 0;
       dp.num_reqs = num_reqs;
-      dp.num_units = num_reqs;
+      dp.unit_tokens = short_unit_tokens(G);
+      dp.groups_per_req = (int)cdivll(kShortRequestQueries, dp.unit_tokens);
+      dp.small_max = kShortRequestQueries;
+      dp.num_tokens = num_tokens;
+      if ((long long)num_reqs * dp.groups_per_req * num_kv_heads * kShortRequestMaxSplits > (1ll << 31) - 1)
+        return PA_ERR_UNSUPPORTED;
+      dp.num_units = num_reqs * dp.groups_per_req;
       dp.num_q_heads = num_q_heads;
       dp.num_kv_heads = num_kv_heads;
       dp.group = G;
@@ -543,7 +568,7 @@ extern "C" pa_status pa_paged_attention_varlen_strided(const void* q, const void
       if (st != PA_OK) return st;
     }
     VarlenParams vp{};
-    vp.skip_single = split_decodes ? 1 : 0;
+    vp.skip_upto = split_decodes ? kShortRequestQueries : 0;
     vp.query_start_loc = query_start_loc;
     vp.seq_lens = seq_lens;
     vp.block_tables = block_tables;

@@ -28,9 +28,14 @@ struct DecodeParams {
   float* ws_acc;  // [units, splits, Hq, D] when num_splits > 1
   float* ws_ml;   // [units, splits, Hq, 2]
   int32_t* err;
-  // units: 0 = sequences (decode); 1 = the query tokens of varlen requests; 2 = varlen requests,
-  // only those with exactly one query (the others are skipped: nothing is written for them)
+  // units: 0 = sequences (decode); 1 = the query tokens of varlen requests; 2 = groups of up to
+  // unit_tokens consecutive queries of the varlen requests with 1 <= q_len <= small_max
+  // (groups_per_req units per request; the other requests are skipped: nothing is written)
   int varlen;
+  int unit_tokens;     // queries per unit (1 unless varlen == 2); rows = unit_tokens * group
+  int groups_per_req;  // varlen == 2
+  int small_max;       // varlen == 2
+  int num_tokens;      // varlen == 2: rows of q / out (query blocks reaching past them are skipped)
   int causal;
   int num_reqs;
   int num_units;
@@ -117,8 +122,9 @@ struct VarlenParams {
   // slot t * slot_count + r of ws_acc / ws_ml instead of `out`
   int prefix_mode;
   const int32_t* prefix_len;
-  // requests with exactly one query are left to the split-KV decode (launched beside this kernel)
-  int skip_single;
+  // requests with 1 <= q_len <= skip_upto are left to the split-KV decode (launched beside this
+  // kernel); 0 = none
+  int skip_upto;
   int prefix_tiles_per_split;
   float* ws_acc;
   float* ws_ml;

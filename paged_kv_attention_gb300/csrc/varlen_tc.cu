@@ -255,8 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     q_start = p.query_start_loc[r];
     q_stop = p.query_start_loc[r + 1];
     seq_len = p.seq_lens[r];
-    // one-query requests left to the split-KV decode launched beside this kernel
-    if (p.skip_single && q_stop - q_start == 1 && q_start >= 0) return;
+    // short requests (decodes, verify blocks) left to the split-KV decode launched beside it
+    // (a malformed block, reaching past the last row, stays here to be flagged)
+    if (q_start >= 0 && q_stop <= p.num_tokens && q_stop - q_start >= 1 && q_stop - q_start <= p.skip_upto) return;
   }
   const int q_len = q_stop - q_start;
   const bool layout_ok = q_start >= 0 && q_len >= 0 && q_stop <= p.num_tokens;

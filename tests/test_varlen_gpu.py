@@ -166,6 +166,65 @@ def test_one_query_requests_on_either_path(split_decodes, hq, hkv, bs):
                 label=f"split_decodes={split_decodes} G{hq // hkv} bs{bs}")
 
 
+SHORT_Q = [2, 1, 5, 8, 9, 3, 64, 4, 7, 6]          # 9 and 64: past the short limit (8 queries)
+SHORT_SEQ = [2, 3000, 900, 2500, 800, 40, 300, 4096, 17, 129]
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 2, 64), (16, 1, 32), (8, 8, 16), (8, 4, 128)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_short_requests_on_the_split_path(hq, hkv, bs, causal):
+    """Requests of up to 8 queries (decodes, verify blocks) go to the split-KV decode in units of
+    up to 16 query rows, each query seeing its own causal range; the rest of the batch stays on
+    the tensor-core kernel. Every short request's every query is checked against the oracle."""
+    case = workloads.make_case("vshort", 300 + hq + hkv + bs, SHORT_Q, SHORT_SEQ, num_q_heads=hq, num_kv_heads=hkv,
+                               head_dim=128, block_size=bs, dtype=torch.bfloat16, causal=causal)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_varlen(case, kc, vc, split_decodes=True, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = sample_tokens(case)
+    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), torch.bfloat16, rows=rows,
+                label=f"short requests G{hq // hkv} bs{bs} causal={causal}")
+    # the same batch without the split path: the same rows within the tolerance of both paths
+    ref = run_varlen(case, kc, vc, split_decodes=False)
+    assert (out.float() - ref.float()).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("window,softcap,sinks", [(100, 0.0, False), (0, 30.0, False), (0, 0.0, True),
+                                                  (37, 20.0, True)])
+def test_short_requests_with_score_modifiers(window, softcap, sinks):
+    case = workloads.make_case("vshortm", 411 + window, SHORT_Q, SHORT_SEQ, num_q_heads=32, num_kv_heads=8,
+                               head_dim=128, block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    sk = torch.linspace(-2.0, 3.0, 32, dtype=torch.float32) if sinks else None
+    out = run_varlen(case, kc, vc, split_decodes=True, window=window, softcap=softcap,
+                     sinks=None if sk is None else sk.to(DEV))
+    rows = sample_tokens(case)
+    want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, case.seq_lens, case.block_tables,
+                                         True, case.scale, tokens=rows, window=window, softcap=softcap, sinks=sk)
+    check_close(out, want, torch.bfloat16, rows=rows, label=f"short w{window} cap{softcap} sinks{sinks}")
+
+
+def test_short_request_without_its_positions_is_flagged_on_the_split_path():
+    case = workloads.make_case("vse", 99, [3, 4], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    lens = case.seq_lens.clone()
+    lens[0] = 2                                       # three queries but only two cached positions
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pa.paged_attention_varlen(case.q.to(DEV), kc, vc, case.query_start_loc.to(DEV), lens.to(DEV),
+                                    case.block_tables.to(DEV), case.max_query_len, True, case.scale,
+                                    error_word=err, split_decodes=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa._lib.PA_ERRBIT_QUERY_LAYOUT
+    assert torch.equal(out[:3].float(), torch.zeros_like(out[:3].float()))
+    ko, vo = oracle_pools(case)
+    check_close(out[3:], oracle_varlen(case, ko, vo)[3:], torch.bfloat16, label="clean request")
+
+
 def test_one_query_request_without_its_position_is_flagged():
     case = workloads.make_case("v1e", 98, [1, 3], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
                                block_size=16, dtype=torch.bfloat16)
