@@ -4,7 +4,8 @@
 // "32. Production attention kernels", Long contexts: split the keys):
 //  * one CTA per (unit, KV head, split); the query heads that share the KV head form the
 //    rows of one query tile, so every page of keys and values is read from HBM once per
-//    group;
+//    group (a unit of several queries, a short varlen request, stacks their groups: rows =
+//    queries x group, each row masked to its own query's causal range);
 //  * the CTA walks its share of the block table 16 tokens at a time: a producer warp reads
 //    the page id (a scalar load) and issues TMA loads of that page's rows for this KV head
 //    into a ring of shared-memory stages;
@@ -321,9 +322,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Decode (one query per unit): the block-table row is the unit, and this split's first
-  // page is known before its length is, so the producer starts its first page-id window load
-  // now and the two memory latencies overlap. (A window that turns out to start later than
+  // Decode and request units: the block-table row follows from the unit alone, and this split's
+  // first page is known before its length is, so the producer starts its first page-id window
+  // load now and the two memory latencies overlap. (A window that turns out to start later than
   // the split is simply reloaded.)
   int spec_base = -64, spec_page = -1;
   if (warp >= C::kConsumers && lane == 0) {

@@ -14,8 +14,9 @@ constexpr int kMaxSplits = 32;
 constexpr int kChunk = 16;  // tokens per decode pipeline stage
 
 // Everything a decode-style kernel needs. A "unit" is one query row set that shares a
-// context: a sequence (decode) or a single query token of a varlen request (varlen
-// generic path). Work is grid (unit * num_splits + split, kv head).
+// context: a sequence (decode), a single query token of a varlen request (varlen generic
+// path) or a group of consecutive queries of a short varlen request. Work is grid
+// (unit * num_splits + split, kv head).
 struct DecodeParams {
   const void* q;
   const void* k_cache;
