@@ -461,6 +461,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         key_hi[nt][j] = p.causal ? u.len - (u.n_tok - 1 - t) : u.len;
         key_lo[nt][j] = p.window > 0 ? u.first_pos + t - p.window + 1 : 0;
       }
+    // keys in [all_lo, all_hi) are visible to every row: chunks inside need no mask at all
+    const int all_hi = p.causal ? u.len - (u.n_tok - 1) : u.len;
+    const int all_lo = p.window > 0 ? u.first_pos + u.n_tok - p.window : 0;
     float o[NT][C::kMT][4];
     float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -585,7 +588,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         } else {
           x0 = s[nt][0] * sl2, x1 = s[nt][1] * sl2, x2 = s[nt][2] * sl2, x3 = s[nt][3] * sl2;
         }
-        {
+        if (key0 + kChunk > all_hi || key0 < all_lo) {  // uniform: the sequence's ends only
           const int ka = key0 + g4, kb = ka + 8;  // positions of this thread's two keys
           if (ka >= key_hi[nt][0] || ka < key_lo[nt][0]) x0 = -INFINITY;
           if (ka >= key_hi[nt][1] || ka < key_lo[nt][1]) x1 = -INFINITY;
