@@ -225,6 +225,33 @@ def test_short_request_without_its_positions_is_flagged_on_the_split_path():
     check_close(out[3:], oracle_varlen(case, ko, vo)[3:], torch.bfloat16, label="clean request")
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (12, 4), (8, 8)])   # group 4, group 3, MHA
+@pytest.mark.parametrize("window", [0, 24])
+def test_milestone_batch_matches_each_request_alone(hq, hkv, window):
+    """The milestone batch of 32. Production attention kernels, "The tests and the measurements": a prefill
+    chunk in the middle of its prompt, a whole 16-token prompt, a 21-token prompt and decodes at
+    70 and 130 cached tokens, in one batch. Every row matches the oracle, and every request's rows
+    equal (bit for bit) what the same call gives for that request alone."""
+    q_lens = [32, 16, 21, 1, 1]
+    seq_lens = [72, 16, 21, 70, 130]
+    case = workloads.make_case("milestone", 500 + hq + window, q_lens, seq_lens, num_q_heads=hq, num_kv_heads=hkv,
+                               head_dim=128, block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    out = run_varlen(case, kc, vc, window=window)
+    want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, case.seq_lens, case.block_tables,
+                                         True, case.scale, window=window)
+    check_close(out, want, torch.bfloat16, label=f"milestone Hq{hq} Hkv{hkv} w{window}")
+    qsl = case.query_start_loc.tolist()
+    for r in range(len(q_lens)):
+        a, b = qsl[r], qsl[r + 1]
+        solo = pa.paged_attention_varlen(case.q[a:b].to(DEV), kc, vc,
+                                         torch.tensor([0, b - a], dtype=torch.int32, device=DEV),
+                                         case.seq_lens[r:r + 1].to(DEV), case.block_tables[r:r + 1].to(DEV),
+                                         case.max_query_len, True, case.scale, window=window)
+        assert torch.equal(solo, out[a:b]), f"request {r} differs alone"
+
+
 def test_one_query_request_without_its_position_is_flagged():
     case = workloads.make_case("v1e", 98, [1, 3], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
                                block_size=16, dtype=torch.bfloat16)
