@@ -112,6 +112,15 @@ def test_workspace_bytes(lib):
     assert f(0, 32, 128, 16, 16, 0) == 0
 
 
+def test_varlen_workspace_bytes(lib):
+    f = lib.pa_varlen_workspace_bytes
+    # short requests: 8 query rows each, at most 8 splits (never more than the 16-token chunks)
+    assert f(64, 32, 128, 256, 16) == 64 * 8 * 8 * 32 * 130 * 4
+    assert f(4, 8, 64, 2, 16) == 4 * 8 * 2 * 8 * 66 * 4          # 2 chunks: at most 2 splits
+    assert f(4, 8, 64, 1, 16) == 0                                # one chunk: one split, no partials
+    assert f(0, 8, 64, 16, 16) == 0
+
+
 def _decode_args(**over):
     a = dict(q=16, k=16, v=16, tables=16, lens=16, S=1, Hq=8, Hkv=2, D=128, bs=16, nb=4, mb=16,
              scale=0.0, dtype=_lib.PA_DTYPE_BF16, splits=0, out=16, ws=None, ws_bytes=0, err=None, stream=None)
