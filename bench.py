@@ -645,6 +645,15 @@ def configs_leg(args, dev, peaks):
         "us_median": round(med, 2), "us_min": round(mn, 2), "causal_flops": flops, "kv_bytes": kv,
         "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
         "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
+    # the same batch on a host-planned grid (pa_varlen_plan on the host copies of the lengths, the
+    # items copied to the device once; the plan itself is host work outside the timed call)
+    items = pa.varlen_plan(case.query_start_loc, case.seq_lens, case.max_query_len, case.num_q_heads,
+                           case.num_kv_heads, True).to(dev)
+    med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o, work_items=items))
+    res["varlen_mixed_bf16_planned"] = {
+        "us_median": round(med, 2), "us_min": round(mn, 2), "items": int(items.numel()),
+        "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
+        "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
     return res
 
 

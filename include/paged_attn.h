@@ -306,6 +306,49 @@ pa_status pa_paged_attention_varlen_strided(const void* q, const void* k_cache, 
                                             const pa_row_strides* strides, void* workspace,
                                             size_t workspace_bytes, int32_t* error_word, void* stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Planned varlen grid. The tensor-core kernel's default grid is every (query tile pair,
+ * request, KV head) up to max_query_len, heaviest tile index first; CTAs of pairs a request does
+ * not have exit at once but still take an SM slot (about 0.8 us each: 3,136 of the mixed
+ * workload's 4,096 CTAs). A caller that knows its batch on the host (a serving engine builds
+ * query_start_loc and seq_lens there) can plan instead: pa_varlen_plan lists only the pairs that
+ * exist, longest first by their key tiles, and pa_paged_attention_varlen_planned runs exactly
+ * those. ("TileInfer.jl - Attention kernels", Open questions: the heaviest causal blocks first.)
+ * --------------------------------------------------------------------------------------- */
+
+/* Upper bound on the items of a plan: cdiv(max_query_len, 2 * 128 / G) * num_reqs; -1 for bad
+ * arguments (G = num_q_heads / num_kv_heads must be 1..16). Host only. */
+int pa_varlen_plan_capacity(int num_reqs, int max_query_len, int num_q_heads, int num_kv_heads);
+
+/* Host only: fill work_items (host memory, `capacity` entries) with the batch's (tile pair,
+ * request) items, item = tile * num_reqs + request, ordered by descending key tiles of the
+ * pair's longer tile. query_start_loc [num_reqs + 1] and seq_lens [num_reqs] are HOST copies of
+ * what the call will read on the device; causal and sliding_window as in the call. Requests with
+ * 1 <= q_len <= skip_upto are left out: pass 8 when the call gets a workspace (those requests then
+ * go to the split-KV decode; see pa_paged_attention_varlen_ws), 0 otherwise. Returns the number of
+ * items, or -1 for bad arguments or too small a capacity. The caller copies the items to the
+ * device. */
+int pa_varlen_plan(const int32_t* query_start_loc, const int32_t* seq_lens, int num_reqs, int max_query_len,
+                   int num_q_heads, int num_kv_heads, int causal, int sliding_window, int skip_upto,
+                   int32_t* work_items, int capacity);
+
+/* pa_paged_attention_varlen_strided on a planned grid: work_items is a DEVICE copy of
+ * pa_varlen_plan's output (num_items entries; NULL = the default grid). The plan must come from
+ * the same batch: an item naming a tile past max_query_len is flagged (PA_ERRBIT_QUERY_LAYOUT)
+ * and skipped, a request left out of the plan gets no rows. Same results as the default grid,
+ * bit for bit (each pair's CTA computes the same thing, only the order changes). */
+pa_status pa_paged_attention_varlen_planned(const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* query_start_loc, const int32_t* seq_lens,
+                                            const int32_t* block_tables,
+                                            int num_reqs, int num_tokens, int max_query_len,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int num_blocks, int max_blocks_per_seq,
+                                            int causal, float scale, pa_dtype dtype,
+                                            void* out, const pa_attn_options* options,
+                                            const pa_row_strides* strides, void* workspace,
+                                            size_t workspace_bytes, const int32_t* work_items, int num_items,
+                                            int32_t* error_word, void* stream);
+
 /* Workspace bytes pa_paged_attention_varlen_ws needs: the split partials of num_reqs short
  * requests (8 queries per request, at most 8 splits): num_reqs * 8 * min(8, chunks) * Hq *
  * (D + 2) * 4 with chunks = cdiv(max_blocks_per_seq * block_size, 16); 0 when one split covers

@@ -178,6 +178,30 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+SHORT_REQUEST_QUERIES = 8  # requests of at most this many queries go to the split-KV decode
+
+
+def varlen_plan(query_start_loc: torch.Tensor, seq_lens: torch.Tensor, max_query_len: int, num_q_heads: int,
+                num_kv_heads: int, causal: bool = True, window: int = 0, split_decodes: bool = False) -> torch.Tensor:
+    """Host plan of the tensor-core grid for one batch (pa_varlen_plan): the (tile pair, request)
+    items that exist, longest first, as a CPU int32 tensor to copy to the device and pass as
+    ``work_items``. ``split_decodes`` must match the call's."""
+    qsl = query_start_loc.to("cpu", torch.int32).contiguous()
+    sl = seq_lens.to("cpu", torch.int32).contiguous()
+    r = sl.shape[0]
+    lib = _lib.load()
+    cap = int(lib.pa_varlen_plan_capacity(r, int(max_query_len), num_q_heads, num_kv_heads))
+    if cap < 0:
+        raise PagedAttentionError("pa_varlen_plan_capacity", _lib.PA_ERR_INVALID_ARGUMENT)
+    items = torch.empty(max(cap, 1), dtype=torch.int32)
+    n = int(lib.pa_varlen_plan(qsl.data_ptr(), sl.data_ptr(), r, int(max_query_len), num_q_heads, num_kv_heads,
+                               int(bool(causal)), int(window), SHORT_REQUEST_QUERIES if split_decodes else 0,
+                               items.data_ptr(), cap))
+    if n < 0:
+        raise PagedAttentionError("pa_varlen_plan", _lib.PA_ERR_INVALID_ARGUMENT)
+    return items[:n]
+
+
 def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
                            block_tables: torch.Tensor, max_query_len: int, causal: bool = True,
@@ -185,7 +209,7 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            error_word: torch.Tensor | None = None,
                            stream: torch.cuda.Stream | None = None, window: int = 0, softcap: float = 0.0,
                            sinks: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                           split_decodes: bool = False) -> torch.Tensor:
+                           split_decodes: bool = False, work_items: torch.Tensor | None = None) -> torch.Tensor:
     """Flattened prefill / verify / decode batch; request r's queries are the newest q_len of
     its seq_lens[r] positions, causal by position. ``window``, ``softcap`` and ``sinks`` are
     the pa_attn_options score modifiers. With ``split_decodes`` (bf16), the batch's short
@@ -206,7 +230,16 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         workspace = None
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
     strides = _strides(q, out)
-    if strides is None:
+    if work_items is not None:
+        if work_items.dtype != torch.int32 or not work_items.is_cuda:
+            raise ValueError("work_items must be an int32 CUDA tensor (varlen_plan's output, copied)")
+        st = lib.pa_paged_attention_varlen_planned(
+            _row_ptr(q)[0], _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+            _ptr(block_tables), r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)),
+            float(scale or 0.0), _dtype(q), _row_ptr(out)[0], _options(window, softcap, sinks), strides,
+            _ptr(workspace), ws_len, _ptr(work_items) if work_items.numel() else 16, int(work_items.numel()),
+            _ptr(error_word), _stream(stream))
+    elif strides is None:
         st = lib.pa_paged_attention_varlen_ws(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
             r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)), float(scale or 0.0),

@@ -80,6 +80,10 @@ SIGNATURES = {
                                                _p, _p, _sz, _opt, _rs, _p, _p]),
     "pa_paged_attention_varlen_strided": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                                _i, _f, _i, _p, _opt, _rs, _p, _sz, _p, _p]),
+    "pa_varlen_plan_capacity": (_i, [_i, _i, _i, _i]),
+    "pa_varlen_plan": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _i]),
+    "pa_paged_attention_varlen_planned": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                               _i, _f, _i, _p, _opt, _rs, _p, _sz, _p, _i, _p, _p]),
 }
 
 _lib = None

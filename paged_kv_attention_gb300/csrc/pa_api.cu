@@ -2,8 +2,10 @@
 // launches on the caller's stream. Nothing here allocates device memory or synchronises.
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -513,7 +515,73 @@ extern "C" pa_status pa_paged_attention_varlen_strided(const void* q, const void
                                                        pa_dtype dtype, void* out, const pa_attn_options* options,
                                                        const pa_row_strides* strides, void* workspace,
                                                        size_t workspace_bytes, int32_t* error_word, void* stream) {
+  return pa_paged_attention_varlen_planned(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, num_reqs,
+                                           num_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim,
+                                           block_size, num_blocks, max_blocks_per_seq, causal, scale, dtype, out,
+                                           options, strides, workspace, workspace_bytes, nullptr, -1, error_word,
+                                           stream);
+}
+
+extern "C" int pa_varlen_plan_capacity(int num_reqs, int max_query_len, int num_q_heads, int num_kv_heads) {
+  if (num_reqs < 0 || max_query_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+    return -1;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > 16) return -1;
+  const long long n = cdivll(max_query_len, varlen_tc_tokens_per_cta(G)) * (long long)num_reqs;
+  return n > (1ll << 31) - 1 ? -1 : (int)n;
+}
+
+extern "C" int pa_varlen_plan(const int32_t* query_start_loc, const int32_t* seq_lens, int num_reqs,
+                              int max_query_len, int num_q_heads, int num_kv_heads, int causal, int sliding_window,
+                              int skip_upto, int32_t* work_items, int capacity) {
+  const int cap_needed = pa_varlen_plan_capacity(num_reqs, max_query_len, num_q_heads, num_kv_heads);
+  if (cap_needed < 0 || sliding_window < 0 || skip_upto < 0 || capacity < 0) return -1;
+  if (num_reqs == 0) return 0;
+  if (!query_start_loc || !seq_lens || !work_items) return -1;
+  const int G = num_q_heads / num_kv_heads;
+  const int TOK = 128 / G;                       // tokens of one 128-row query tile
+  const int per_cta = varlen_tc_tokens_per_cta(G);  // a CTA's two tiles
+  const int q_tiles = (int)cdivll(max_query_len, per_cta);
+  // key tiles (128 keys) the query tile [tok0, tok0 + n) of a request walks
+  auto key_tiles = [&](int q_len, int seq, int tok0) {
+    const int n = std::max(0, std::min(TOK, q_len - tok0));
+    if (n == 0) return 0;
+    const int first = seq - q_len + tok0;
+    const int key_end = causal ? std::min(seq, first + n) : seq;
+    const int j0 = sliding_window > 0 ? std::max(0, first - sliding_window + 1) / 128 : 0;
+    return std::max(0, (int)cdivll(std::max(0, key_end), 128) - j0);
+  };
+  struct Item {
+    int work;
+    int32_t id;
+  };
+  std::vector<Item> items;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int q_len = query_start_loc[r + 1] - query_start_loc[r];
+    if (q_len <= 0 || q_len <= skip_upto) continue;  // nothing here, or served by the split-KV decode
+    const int seq = seq_lens[r];
+    const int tiles = std::min((int)cdivll(q_len, per_cta), q_tiles);
+    for (int t = 0; t < tiles; ++t) {
+      const int tok0 = t * per_cta;
+      const int work = std::max(key_tiles(q_len, seq, tok0), key_tiles(q_len, seq, tok0 + TOK));
+      items.push_back({work, (int32_t)(t * num_reqs + r)});
+    }
+  }
+  if ((long long)items.size() > capacity) return -1;
+  // longest first (a CTA's time is about proportional to its key tiles), ties in request order
+  std::stable_sort(items.begin(), items.end(), [](const Item& a, const Item& b) { return a.work > b.work; });
+  for (size_t i = 0; i < items.size(); ++i) work_items[i] = items[i].id;
+  return (int)items.size();
+}
+
+extern "C" pa_status pa_paged_attention_varlen_planned(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* block_tables, int num_reqs, int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
+    void* out, const pa_attn_options* options, const pa_row_strides* strides, void* workspace, size_t workspace_bytes,
+    const int32_t* work_items, int num_items, int32_t* error_word, void* stream) {
   if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
+  if (work_items != nullptr && num_items < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_reqs == 0 || num_tokens == 0) return PA_OK;
   if (!query_start_loc || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
   pa_status st = validate_common(q, k_cache, v_cache, block_tables, out, num_q_heads, num_kv_heads, head_dim,
@@ -584,6 +652,8 @@ extern "C" pa_status pa_paged_attention_varlen_strided(const void* q, const void
     vp.max_blocks = max_blocks_per_seq;
     vp.max_query_len = max_query_len;
     vp.out_stride = out_stride;
+    vp.work_items = work_items;
+    vp.num_items = work_items != nullptr ? num_items : 0;
     const int tokens_per_tile = 128 / G;
     vp.q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
     vp.causal = causal ? 1 : 0;

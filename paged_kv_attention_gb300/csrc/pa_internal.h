@@ -133,6 +133,10 @@ struct VarlenParams {
   // elements from one token's output row to the next; 0 = dense (Hq * D). The query row stride
   // is carried by the query tensor map.
   long long out_stride;
+  // planned grid: CTA i serves item work_items[i / num_kv_heads] = tile * num_reqs + request
+  // (nullptr: every tile of every request, heaviest tile index first)
+  const int32_t* work_items;
+  int num_items;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
 int varlen_tc_tokens_per_cta(int group);

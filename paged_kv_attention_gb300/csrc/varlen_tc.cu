@@ -230,12 +230,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* issued_tiles = reinterpret_cast<int*>(tmem_slot + 2);
 
-  // ---- which tile pair: heaviest (last) query tiles first across all requests and heads
-  const int per_tile = p.num_reqs * p.num_kv_heads;
-  const int tile = p.q_tiles - 1 - (int)(blockIdx.x / per_tile);
-  const int rem = (int)(blockIdx.x % per_tile);
-  const int r = rem / p.num_kv_heads;  // the request, or the prefix key range in prefix mode
-  const int kvh = rem - r * p.num_kv_heads;
+  // ---- which tile pair: from the caller's plan (heaviest first by the host's estimate, no empty
+  // pairs), else heaviest (last) query tiles first across all requests and heads
+  int tile, r, kvh;  // r: the request, or the prefix key range in prefix mode
+  if (!kPrefix && p.work_items != nullptr) {
+    const int item = __ldg(p.work_items + blockIdx.x / p.num_kv_heads);
+    kvh = (int)(blockIdx.x % p.num_kv_heads);
+    tile = item / p.num_reqs;
+    r = item - tile * p.num_reqs;
+    if (item < 0 || tile >= p.q_tiles) {  // not an item of this batch: nothing to do here
+      if (threadIdx.x == 0 && kvh == 0) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
+      return;
+    }
+  } else {
+    const int per_tile = p.num_reqs * p.num_kv_heads;
+    tile = p.q_tiles - 1 - (int)(blockIdx.x / per_tile);
+    const int rem = (int)(blockIdx.x % per_tile);
+    r = rem / p.num_kv_heads;
+    kvh = rem - r * p.num_kv_heads;
+  }
   const int G = p.group;
   const int TOK = kBM / G;  // tokens per 128-row tile; a CTA covers 2 * TOK tokens
   const int tid = threadIdx.x;
@@ -700,7 +713,9 @@ cudaError_t launch_varlen_tc(const VarlenParams& p_in, const CUtensorMap& qmap, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev][mode].store(true, std::memory_order_release);
   }
-  const long long ctas = (long long)p.q_tiles * p.num_reqs * p.num_kv_heads;
+  const long long ctas = (p.work_items != nullptr && !p.prefix_mode ? (long long)p.num_items
+                                                                     : (long long)p.q_tiles * p.num_reqs) *
+                         p.num_kv_heads;
   if (ctas <= 0) return cudaSuccess;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(p, qmap, kmap, vmap);

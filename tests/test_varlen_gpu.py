@@ -252,6 +252,48 @@ def test_milestone_batch_matches_each_request_alone(hq, hkv, window):
         assert torch.equal(solo, out[a:b]), f"request {r} differs alone"
 
 
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("window", [0, 700])
+def test_planned_grid_equals_default_grid(split, window):
+    """pa_varlen_plan + pa_paged_attention_varlen_planned: only the pairs the batch has, longest
+    first. Each pair's CTA computes what it computes on the default grid: bitwise equal."""
+    case, _ = named_case("varlen_mixed_bf16")
+    kc, vc = gpu_pools(case)
+    items = pa.varlen_plan(case.query_start_loc, case.seq_lens, case.max_query_len, case.num_q_heads,
+                           case.num_kv_heads, case.causal, window, split_decodes=split)
+    assert 0 < items.numel() < case.num_reqs * -(-case.max_query_len // 64)
+    base = run_varlen(case, kc, vc, split_decodes=split, window=window)
+    planned = run_varlen(case, kc, vc, split_decodes=split, window=window, work_items=items.to(DEV))
+    assert torch.equal(base, planned)
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 1, 64), (8, 8, 128), (16, 2, 32)])
+def test_planned_small_batches(hq, hkv, bs):
+    q_lens, seq_lens = [1, 64, 0, 37, 130, 5, 300], [700, 100, 3, 37, 900, 5, 2000]
+    case = workloads.make_case("vplan", 700 + hq + bs, q_lens, seq_lens, num_q_heads=hq, num_kv_heads=hkv,
+                               head_dim=128, block_size=bs, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    items = pa.varlen_plan(case.query_start_loc, case.seq_lens, case.max_query_len, hq, hkv)
+    out = run_varlen(case, kc, vc, work_items=items.to(DEV))
+    assert torch.equal(out, run_varlen(case, kc, vc))
+    rows = sample_tokens(case)
+    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), torch.bfloat16, rows=rows, label="planned")
+
+
+def test_plan_item_outside_the_batch_is_flagged():
+    case = workloads.make_case("vplanbad", 77, [40, 3], [40, 10], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    items = pa.varlen_plan(case.query_start_loc, case.seq_lens, case.max_query_len, 8, 2)
+    bad = torch.cat([items, torch.tensor([99 * case.num_reqs], dtype=torch.int32)]).to(DEV)  # tile 99
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_varlen(case, kc, vc, work_items=bad, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa._lib.PA_ERRBIT_QUERY_LAYOUT
+    assert torch.equal(out, run_varlen(case, kc, vc))
+
+
 def test_one_query_request_without_its_position_is_flagged():
     case = workloads.make_case("v1e", 98, [1, 3], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
                                block_size=16, dtype=torch.bfloat16)
