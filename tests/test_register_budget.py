@@ -14,6 +14,13 @@ from paged_kv_attention_gb300 import build
 SRC = os.path.join(os.path.dirname(build.__file__), "csrc", "decode.cu")
 
 
+def have_nvcc():
+    try:
+        return bool(build.nvcc())
+    except RuntimeError:
+        return False
+
+
 def ptxas_registers(src):
     with tempfile.TemporaryDirectory() as d:
         r = subprocess.run([build.nvcc(), *build._flags(False), "-Xptxas", "-v", "-c", src,
@@ -31,7 +38,7 @@ def ptxas_registers(src):
     return regs
 
 
-@pytest.mark.skipif(build.nvcc() is None, reason="no nvcc")
+@pytest.mark.skipif(not have_nvcc(), reason="no nvcc")
 def test_bf16_decode_keeps_three_ctas_per_sm():
     regs = ptxas_registers(SRC)
     name = next(k for k in regs if "decode_tc_kernelILi128ELi1ELi0E" in k)
