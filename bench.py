@@ -620,6 +620,7 @@ def configs_leg(args, dev, peaks):
         elt = 4 if case.dtype == torch.float32 else 2
         kv = sum(int(x) for x in case.seq_lens) * Hkv * D * elt * 2
         entry = {"us_median": round(med, 2), "us_min": round(mn, 2), "splits": splits, "kv_bytes": kv,
+                 "queries_per_s": round(S / (med * 1e-6)),
                  "GBps": round(kv / med / 1e3, 1), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
         if name != "decode_64x4096_bf16_d256":
             emed, emn = timed(call, graph=False)
@@ -643,6 +644,7 @@ def configs_leg(args, dev, peaks):
     kv = sum(sls) * case.num_kv_heads * case.head_dim * 2 * 2
     res["varlen_mixed_bf16"] = {
         "us_median": round(med, 2), "us_min": round(mn, 2), "causal_flops": flops, "kv_bytes": kv,
+        "queries_per_s": round(case.num_tokens / (med * 1e-6)),
         "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
         "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
     # the same batch on a host-planned grid (pa_varlen_plan on the host copies of the lengths, the
@@ -652,6 +654,7 @@ def configs_leg(args, dev, peaks):
     med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o, work_items=items))
     res["varlen_mixed_bf16_planned"] = {
         "us_median": round(med, 2), "us_min": round(mn, 2), "items": int(items.numel()),
+        "queries_per_s": round(case.num_tokens / (med * 1e-6)),
         "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
         "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
     return res
@@ -755,6 +758,7 @@ def main():
             "value": round(d["e2e_value"], 2), "unit": "GB/s", "h2d_bytes_per_step": d["h2d"],
             "d2h_bytes_per_step": d["d2h"]},
         "gpu_launches": d["launches"],
+        "decode_queries_per_s": round(world * case.num_reqs / (d["call_ms"] * 1e-3)),
         "clocks": clk,
     }
     if p is not None:
