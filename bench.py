@@ -801,6 +801,14 @@ def main():
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{n} of 64 sequences (full 4096-token contexts, all 32 heads), "
                                           f"{dt:.1f} s"}
+        # the same oracle on one host thread (a bounded sample of a few sequences)
+        torch.set_num_threads(1)
+        try:
+            v1, dt1, n1, _ = time_oracle_decode(case, *ko_vo, budget_s=4.0, max_seqs=4)
+        finally:
+            torch.set_num_threads(threads)
+        line["cpu_baseline"]["one_thread"] = {"value": round(v1, 4), "unit": "GB/s",
+                                              "sample": f"{n1} sequences, {dt1:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
