@@ -700,6 +700,9 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   }
   __syncthreads();
   merge_and_store<__nv_bfloat16>(p, merge_o, merge_ml, C::kConsumers, ROWS, D, unit, u, kvh, split);
+  // launched to overlap the previous kernel (which this one does not read): finish only after it
+  // (a no-op for an ordinary launch)
+  if (p.overlap_previous) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ fp32 CUDA-core decode
@@ -947,8 +950,22 @@ cudaError_t launch_tc_impl(const DecodeParams& p, const CUtensorMap& kmap, const
     if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
   dim3 grid((unsigned)(p.num_units * p.num_splits), (unsigned)p.num_kv_heads, 1);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, kmap, vmap);
-  return cudaGetLastError();
+  if (!p.overlap_previous) {
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, kmap, vmap);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: the CTAs may start while the previous kernel still runs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, kmap, vmap);
 }
 
 template <int D, int NT, int QK>

@@ -980,6 +980,9 @@ extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const
   p.force_partial = 1;
   p.slot_offset = plan.prefix_splits;
   p.slot_count = slots;
+  // the suffixes read nothing the prefix pass writes: their CTAs may start on the SMs the prefix
+  // pass leaves free, while it runs (they finish only after it, for the combine's sake)
+  p.overlap_previous = 1;
   CUtensorMap skmap, svmap;
   if (!encode_cache_map(&skmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk) ||
       !encode_cache_map(&svmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk))

@@ -67,6 +67,10 @@ struct DecodeParams {
   // elements from one query row (a sequence or token) of q / out to the next; 0 = dense (Hq * D)
   long long q_stride;
   long long out_stride;
+  // 1: launched as a programmatic dependent of the previous kernel on the stream, which it does
+  // not read from; its CTAs wait for that kernel's completion only before they exit, so that
+  // this grid's completion implies the previous one's (the combine after it reads both)
+  int overlap_previous;
 };
 
 // key_stride / value_stride: bytes from one token's row to the next (multiples of 16)

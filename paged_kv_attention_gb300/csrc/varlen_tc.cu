@@ -327,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const int warp = tid >> 5, lane = tid & 31;
+  // a kernel launched to overlap this one (it reads nothing this one writes) may start now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     mbar_init(&bars[B_Q], 1);
     for (int s = 0; s < kStages; ++s) {
