@@ -226,10 +226,12 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // registers (ldmatrix over byte pairs) and are converted there, exactly, to fp16; the key's scale
 // multiplies its scores and the value's scale its probabilities before P.V ("TileInfer.jl -
 // Attention kernels", INT8 cache). The page converts to bf16; here the 16-bit type is fp16, which
-// holds every code exactly and converts from int8 in two instructions per two codes (from bf16 it
-// would take three), so the MMAs for 8-bit caches run in fp16 with fp32 accumulation, the queries
-// converted once per CTA (exact within fp16's range) and the probabilities rounded to fp16 (3
-// more mantissa bits than bf16).
+// holds every code exactly, so the MMAs for 8-bit caches run in fp16 with fp32 accumulation, the
+// queries converted once per CTA (exact within fp16's range) and the probabilities rounded to fp16
+// (3 more mantissa bits than bf16). An int8 code c becomes the fp16 1152 + c with one byte permute
+// per two codes; the MMAs take the offset codes and the 1152 offsets are taken out of their sums
+// afterwards (exact up to fp32 rounding of sums some 1152 times larger than the codes'). E4M3
+// codes take one conversion instruction per pair.
 //
 // Register-direct operands rest on two permutations the products do not see. Scores: an
 // ldmatrix of byte pairs hands a thread 4 consecutive codes of a key row, so the k-slots
@@ -281,6 +283,23 @@ __device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w, uint32_t sel) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)pair));
     return h;
   }
+}
+// int8 without the subtraction: two codes of a word already flipped to c + 128 (w ^ 0x80808080)
+// -> the fp16 pair 1152 + c, exactly; one byte permute per two codes. The consumers remove the
+// 1152 offsets after the products: from the scores with the query's dim sum (once per CTA), from
+// P.V with the probability sums that one more MMA against an all-ones operand accumulates.
+__device__ __forceinline__ uint32_t biased2_to_f16x2(uint32_t flipped, uint32_t sel) {
+  return __byte_perm(flipped, 0x64646464u, sel);
+}
+constexpr float kCodeBias = 1152.f;
+constexpr uint32_t kOnesF16x2 = 0x3c003c00u;  // fp16 (1, 1)
+// E4M3: the two code pairs of a word in adjacent bytes (0-1 and 2-3), each a 16-bit half of the
+// word, converted without a byte permute
+__device__ __forceinline__ void e4m3_halves_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 // selectors (result bytes 0 and 2 carry the codes; bytes 1 and 3 take 0x64 from the constant)
 constexpr uint32_t kSelB01 = 0x5140;  // codes in bytes 0, 1
@@ -448,6 +467,25 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         }
       }
     }
+    // int8: 1152 times each score row's query dim sum (rows 2 t4 and 2 t4 + 1 of every 8), the
+    // offset the biased key codes add to its scores; the sum is over the fp16 queries the MMAs use
+    float qb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float part = 0.f;
+      if constexpr (QK == 1) {
+#pragma unroll
+        for (int kk = 0; kk < C::kMT; ++kk) {
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qf[nt][kk][0]));
+          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&qf[nt][kk][1]));
+          part += (a.x + a.y) + (b.x + b.y);
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);  // lanes 4n..4n+3 now hold row n's sum
+      }
+      qb[nt][0] = kCodeBias * __shfl_sync(0xffffffffu, part, 8 * t4);
+      qb[nt][1] = kCodeBias * __shfl_sync(0xffffffffu, part, 8 * t4 + 4);
+    }
     // the keys each of this thread's score rows (2 t4 and 2 t4 + 1 of every 8) may see: query t
     // of the unit sees positions [first_pos + t - window + 1, first_pos + t] when causal (all
     // len when not); a one-query unit's rows all see [start, len)
@@ -466,10 +504,12 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
     const int all_lo = p.window > 0 ? u.first_pos + u.n_tok - p.window : 0;
     float o[NT][C::kMT][4];
     float m_run[NT][2], l_run[NT][2];
+    float psum[NT][4];  // int8: the probability sums of P.V's columns (its offset is 1152 times them)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m_run[nt][0] = m_run[nt][1] = -INFINITY;
       l_run[nt][0] = l_run[nt][1] = 0.f;
+      psum[nt][0] = psum[nt][1] = psum[nt][2] = psum[nt][3] = 0.f;
 #pragma unroll
       for (int mt = 0; mt < C::kMT; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
     }
@@ -548,10 +588,16 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
-      // S^T[16 keys x 8 rows] = K . Q^T
-      float s[NT][4];
+      // S^T[16 keys x 8 rows] = K . Q^T; for E4M3 caches in two accumulator chains (even and odd
+      // 16-dim steps, summed after), which halves the dependent MMA chain of a chunk (for int8 the
+      // four more registers cost more than the shorter chain gains)
+      constexpr int kChains = QK == 2 ? 2 : 1;
+      float s[NT][4], s2[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int nt = 0; nt < NT; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+      }
 #pragma unroll
       for (int kk = 0; kk < C::kMT; ++kk) {
         uint32_t a[4];
@@ -559,20 +605,37 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
           const int dch = kk >> 2;
           const int unit_idx = 2 * (kk & 3) + k_unit;
           ldsm_x4(a, smem_addr(kt + dch * kRegionStride + swz128(k_key, unit_idx)));
+        } else if constexpr (QK == 1) {  // the same slots, biased codes
+          const uint32_t w0 = kw[kk][0] ^ 0x80808080u, w1 = kw[kk][1] ^ 0x80808080u;
+          a[0] = biased2_to_f16x2(w0, kSelB01);
+          a[1] = biased2_to_f16x2(w1, kSelB01);
+          a[2] = biased2_to_f16x2(w0, kSelB23);
+          a[3] = biased2_to_f16x2(w1, kSelB23);
         } else {  // keys g, g+8 x k-slots (2t, 2t+1 | 2t+8, 2t+9) = dims (4t, 4t+1 | 4t+2, 4t+3)
-          a[0] = codes2_to_f16x2<QK>(kw[kk][0], kSelB01);
-          a[1] = codes2_to_f16x2<QK>(kw[kk][1], kSelB01);
-          a[2] = codes2_to_f16x2<QK>(kw[kk][0], kSelB23);
-          a[3] = codes2_to_f16x2<QK>(kw[kk][1], kSelB23);
+          e4m3_halves_to_f16x2(kw[kk][0], a[0], a[2]);
+          e4m3_halves_to_f16x2(kw[kk][1], a[1], a[3]);
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_cache<QK>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+        for (int nt = 0; nt < NT; ++nt)
+          mma_cache<QK>(kChains == 2 && (kk & 1) ? s2[nt] : s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+      }
+      if constexpr (kChains == 2) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
       }
       if constexpr (kLateValues) load_values_and_release();
       // online softmax (rows 2*t4 and 2*t4+1; keys g4 and g4+8)
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
+        if constexpr (QK == 1) {  // the biased keys' offset (columns 2 t4, 2 t4 + 1)
+          s[nt][0] -= qb[nt][0];
+          s[nt][1] -= qb[nt][1];
+          s[nt][2] -= qb[nt][0];
+          s[nt][3] -= qb[nt][1];
+        }
         if constexpr (QK != 0) {  // a key's scale multiplies its scores
           s[nt][0] *= ks_a;
           s[nt][1] *= ks_a;
@@ -615,6 +678,12 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
           const float al1 = up1 ? ex2_ftz(m_run[nt][1] - mu1) : 1.f;
           l_run[nt][0] *= al0;
           l_run[nt][1] *= al1;
+          if constexpr (QK == 1) {
+            psum[nt][0] *= al0;
+            psum[nt][1] *= al1;
+            psum[nt][2] *= al0;
+            psum[nt][3] *= al1;
+          }
 #pragma unroll
           for (int mt = 0; mt < C::kMT; ++mt) {
             o[nt][mt][0] *= al0;
@@ -644,6 +713,12 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
           const int dch = mt >> 2;
           const int unit_idx = 2 * (mt & 3) + v_unit;
           ldsm_x4_trans(a, smem_addr(vt + dch * kRegionStride + swz128(v_key, unit_idx)));
+        } else if constexpr (QK == 1) {  // the same, biased codes
+          const uint32_t w0 = vw[mt][0] ^ 0x80808080u, w1 = vw[mt][1] ^ 0x80808080u;
+          a[0] = biased2_to_f16x2(w0, kSelB02);
+          a[1] = biased2_to_f16x2(w0, kSelB13);
+          a[2] = biased2_to_f16x2(w1, kSelB02);
+          a[3] = biased2_to_f16x2(w1, kSelB13);
         } else {  // rows g, g+8 = dims 2g, 2g+1 of the block x keys (2t, 2t+1 | 2t+8, 2t+9)
           a[0] = codes2_to_f16x2<QK>(vw[mt][0], kSelB02);
           a[1] = codes2_to_f16x2<QK>(vw[mt][0], kSelB13);
@@ -653,10 +728,23 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_cache<QK>(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
+      if constexpr (QK == 1) {  // the same probabilities against all-ones rows: their column sums
+        const uint32_t ones[4] = {kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816_f16(psum[nt], ones, pb[nt][0], pb[nt][1]);
+      }
       if constexpr (QK == 0) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
       }
+    }
+    if constexpr (QK == 1) {  // the biased values' offset
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt][mt][e] -= kCodeBias * psum[nt][e];
     }
     // full row sums: the 8 threads of a row each hold a share of l
 #pragma unroll
