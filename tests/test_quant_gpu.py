@@ -109,3 +109,24 @@ def test_unsupported_head_dim_is_refused():
         pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
                                         case.seq_lens.to(DEV), case.scale)
     assert e.value.status == pa._lib.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_decode_offset_sums_at_their_largest(kind):
+    """The int8 path feeds the MMAs codes offset by 1152 and takes the offsets out of the sums
+    afterwards; those sums are largest when every query dim has one sign (the scores' offset is
+    1152 times the dim sum), the keys are alike (every probability near 1, so the value offset,
+    1152 times the probability sum, grows with the length) and the values fill the code range.
+    8,192 such keys against the float64 attention over the dequantised cache (fp8 alike, as a
+    control)."""
+    case = workloads.decode_case("qo", 750, [8192, 4096, 17, 1], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                 block_size=16, dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(751)
+    case.q = (case.q.float().abs() + 1.0).to(torch.bfloat16)
+    case.key = (1.0 + 0.01 * torch.randn(case.key.shape, generator=g)).to(torch.bfloat16)
+    case.value = (10.0 * torch.randn(case.value.shape, generator=g)).to(torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    out = pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                          case.seq_lens.to(DEV), case.scale, num_splits=1)
+    want = quant.paged_attention_decode_quant(case.q, ko, vo, kso, vso, case.block_tables, case.seq_lens, case.scale)
+    check_close(out, want, torch.bfloat16, label=f"{kind} offset sums")
