@@ -325,24 +325,42 @@ def decode_leg(args, world, rank, dev):
     def decode_call():
         pa.paged_attention_decode(q, kc, vc, tables, ctx, case.scale, num_splits=splits, out=out, workspace=ws)
 
+    def step_calls():
+        write_call()
+        decode_call()
+
     if args.no_graph:
-        run_write, run_call = write_call, decode_call
+        run_write, run_call, run_step = write_call, decode_call, step_calls
     else:
-        # the step's two calls, each captured once and replayed (launch shapes depend only on
+        # the step (both calls) captured once as one graph and replayed, as a serving loop runs
+        # it; each call also captured alone, for the per-call times (launch shapes depend only on
         # host sizes; lengths and positions are read from device buffers at every replay)
         graphs = []
-        for fn in (write_call, decode_call):
+        for fn in (write_call, decode_call, step_calls):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn()
             graphs.append(g)
-        run_write, run_call = graphs[0].replay, graphs[1].replay
+        run_write, run_call, run_step = graphs[0].replay, graphs[1].replay, graphs[2].replay
         for _ in range(3):
             run_write()
             run_call()
+            run_step()
         torch.cuda.synchronize()
+    # per-call times: each call's graph between events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        run_write()
+        ev[i][1].record(stream)
+        run_call()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    call_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    # the timed steps
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -350,19 +368,13 @@ def decode_leg(args, world, rank, dev):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
-        run_write()
-        ev[i][1].record(stream)
-        run_call()
-        ev[i][2].record(stream)
+        run_step()
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t0
     total_ms = start.elapsed_time(end)
     total_ms = max_over_ranks(total_ms, world)
-    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    call_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
 
     call_bytes = decode_call_bytes(lens, Hq, Hkv, D, bs, 2)
     step_bytes = call_bytes + cache_write_bytes(S, Hkv, D, 2)
@@ -377,8 +389,7 @@ def decode_leg(args, world, rank, dev):
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     for _ in range(max(3, args.warmup // 4)):
         din.copy_(hin, non_blocking=True)
-        run_write()
-        run_call()
+        run_step()
         hout.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     barrier(world)
@@ -387,8 +398,7 @@ def decode_leg(args, world, rank, dev):
     e2e_start.record(stream)
     for i in range(args.steps):
         din.copy_(hin, non_blocking=True)
-        run_write()
-        run_call()
+        run_step()
         hout.copy_(out, non_blocking=True)
     e2e_end.record(stream)
     torch.cuda.synchronize()
@@ -744,7 +754,7 @@ def main():
                    "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
                    "block_size": case.block_size, "num_splits": d["splits"],
                    "step": "reshape_and_cache(64 new rows) + decode(split-KV + combine)",
-                   "launch": "eager" if args.no_graph else "CUDA graphs (one per call), replayed each step",
+                   "launch": "eager" if args.no_graph else "one CUDA graph per step (write + decode), replayed; per-call times from one graph per call",
                    "l2": "no flush: 1.07 GB of K/V per step > 129 MB L2",
                    "parallelism": "replicas" if world == 1 else f"dp{world} (independent batches per GPU)"},
         "hbm_frac_of_peak": round(d["value"] / world / hbm, 4),
