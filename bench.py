@@ -5,6 +5,7 @@ One step = one decode step of the memory-bound workload: 64 sequences x 4096 cac
 32 query / 8 KV heads, head_dim 128, block 16, bf16 (1,073,741,824 bytes of K+V):
   1. pa_reshape_and_cache writes the step's 64 new key/value rows into the pools;
   2. pa_paged_attention_decode (split-KV kernel + log-sum-exp combine) answers the 64 queries.
+The two calls are captured as one CUDA graph, replayed once per timed step.
 The headline value is decode HBM throughput: algorithmic bytes (the K/V of every cached
 position read once, q, out, the used block-table entries, the new rows) per second.
 A second leg times causal prefill of 4 x 8192 tokens (block 64): the prompt's cache write
