@@ -420,8 +420,10 @@ pa_status pa_reshape_and_cache_quant(const void* key, const void* value, pa_dtyp
  * values dequantised in registers: codes are converted exactly to fp16 (every int8 code and
  * every E4M3 value is an fp16 value) and the products run in fp16 with fp32 accumulation (q
  * converted to fp16, probabilities rounded to fp16); a key's scale multiplies its scores and a
- * value's scale its probabilities before P.V. Supported: D in {128, 256}, Hq/Hkv <= 16,
- * block_size % 16 == 0. */
+ * value's scale its probabilities before P.V. int8 codes enter the products offset by 1152 (the
+ * fp16 1152 + c, one byte permute per two codes) and the offsets are subtracted from the fp32
+ * sums afterwards, which leaves those sums ~14 significant bits where fp32 has 24 (error of order
+ * 1e-5 of the values' scale). Supported: D in {128, 256}, Hq/Hkv <= 16, block_size % 16 == 0. */
 pa_status pa_paged_attention_decode_quant(const void* q, const void* k_cache, const void* v_cache,
                                           const float* k_scales, const float* v_scales, pa_dtype cache_dtype,
                                           const int32_t* block_tables, const int32_t* context_lens,
