@@ -4,9 +4,9 @@ Random keys give scores whose maximum is reached in the first key tile to within
 so the running reference of the softmax almost never moves. Here every key of 128-key tile i
 gets the same offset level[i] * (1, ..., 1) added, so that a query row's scores shift by
 level[i] * z between tiles (z = scale * sum(q) ~ N(0, 1), either sign): rises of 8-64 octaves
-(the reference moves by a whole number of octaves), rises of more than 64 octaves (it moves to
-the new maximum), and falls. Sinks far below or above the scores make the first tile itself
-such a jump. The oracle follows the textbook softmax in float64, so any reference works for it."""
+and of more than 64 octaves (the reference moves and the accumulated output and row sum are
+rescaled), and falls (the reference stays). Sinks far below or above the scores make the first
+tile itself such a jump. The oracle follows the textbook softmax in float64."""
 
 import pytest
 import torch
