@@ -25,6 +25,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -125,7 +126,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples go to PA_BENCH_LOG_DIR when set (the summary is in the JSON line)
+        log_dir = os.environ.get("PA_BENCH_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
