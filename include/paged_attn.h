@@ -229,7 +229,9 @@ pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const vo
  *     anything is enqueued; pass a smaller num_splits (1 needs no scratch at all).
  *   - The first call on a device, with that device current, looks up the array's device
  *     address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
- *     capture on that device. A failed lookup returns PA_ERR_CUDA.
+ *     capture on that device. A failed lookup returns PA_ERR_CUDA. The address is kept for the
+ *     life of the process and is not looked up again after a device reset (cudaDeviceReset or
+ *     a re-created primary context): calling this entry point across a reset is unsupported.
  *   - Every call on a device shares the one array and it keeps the previous call's contents.
  *     Nothing in it needs to start at zero: each call writes every partial it later reads.
  *     Two calls that overlap on the GPU (e.g. on different streams) race on the array and give

@@ -13,6 +13,12 @@ Test infrastructure only (see the package docstring). Sources, by page title and
 
 The attention itself is the float64 definition in ``attention.attend`` applied to
 code * scale (both exact in float64).
+
+Pins (tests/test_oracle_quant.py): the hand-derived golden quantisation and attention over
+int8 / E4M3 codes (tests/golden/), the quantiser's error bound and range edge, a write/gather
+round trip, and exact agreement (<= 1e-15) of both attention functions with the plain oracle
+over a float64 pool of code * scale, with window, softcap and sinks; planted slips (swapped
+key/value scales, a q_pos = t position rule, a shifted scale gather) fail them.
 """
 
 from __future__ import annotations

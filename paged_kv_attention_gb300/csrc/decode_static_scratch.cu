@@ -12,6 +12,7 @@
 // The array is a file-scope __device__ variable: every GPU that loads the library holds its
 // kStaticScratchBytes for the life of the process. Its address is looked up once per device
 // with cudaGetSymbolAddress (on the first call made while that device is current).
+#include <atomic>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -32,21 +33,26 @@ static __device__ __align__(256) unsigned char pa_decode_static_scratch[kStaticS
 
 namespace {
 
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array on the current device, looked up once per device and
+// kept for the life of the process. After the first lookup a call reads the cached address
+// with one acquire load; only a device's first lookup takes the lock. The cache is not
+// refreshed after a device reset (cudaDeviceReset, or the primary context being released and
+// re-created): the library does not support calling this entry point across one.
 pa_status static_scratch_address(void** out) {
   static std::mutex mu;
-  static void* addr[64] = {};
-  static bool ready[64] = {};
+  static std::atomic<void*> addr[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ready[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, pa_decode_static_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
-    addr[dev] = p;
-    ready[dev] = true;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(mu);
+    p = addr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, pa_decode_static_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+      addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = addr[dev];
+  *out = p;
   return PA_OK;
 }
 
