@@ -121,7 +121,7 @@ def source_hash(source: str) -> str:
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.proc = None
@@ -159,10 +159,14 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) != 9:
+                if len(parts) != 10:
                     continue
                 try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:]))
+                    util = float(parts[9])
+                except ValueError:
+                    util = 0.0
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9], util))
                 except ValueError:
                     continue
         if not rows:
@@ -173,9 +177,13 @@ class ClockSampler:
             for n, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     seen.add(n)
-        loaded = [r for r in rows if r[2] > 250.0] or rows
+        # a sample is under load when a kernel ran for at least half of its 100 ms period
+        under = [r for r in rows if r[4] >= 50.0]
+        loaded = under or rows
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "reasons": sorted(seen), "samples": len(rows)}
+                "power_w_max": max(r[2] for r in rows), "reasons": sorted(seen), "samples": len(rows),
+                "samples_under_load": len(under),
+                "sm_mhz_min_under_load": min((r[0] for r in under), default=None)}
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -351,19 +359,21 @@ def decode_leg(args, world, rank, dev):
             run_call()
             run_step()
         torch.cuda.synchronize()
-    # per-call times: each call's graph between events
+    # per-call times: each call's graph between events, over enough replays (call_reps) that the
+    # clock sampler sees the GPU under load while they run
+    n_rep = max(args.steps, args.call_reps)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+           torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(n_rep):
         ev[i][0].record(stream)
         run_write()
         ev[i][1].record(stream)
         run_call()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    call_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n_rep
+    call_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n_rep
     # the timed steps
     barrier(world)
     torch.cuda.synchronize()
@@ -386,8 +396,8 @@ def decode_leg(args, world, rank, dev):
 
     if args.no_e2e:
         return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
-                    call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=None, h2d=0, d2h=0,
-                    launches=args.steps * (2 + (1 if splits > 1 else 0)))
+                    call_reps=n_rep, call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=None,
+                    h2d=0, d2h=0, launches=args.steps * (2 + (1 if splits > 1 else 0)), out=out.cpu())
     # end to end: host buffers in (one pinned buffer, one copy), the same two calls, the host
     # result out, all inside the timed region
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -411,8 +421,8 @@ def decode_leg(args, world, rank, dev):
     d2h = hout.numel() * hout.element_size()
     e2e_value = whole_job_rate(step_bytes, args.steps, e2e_ms, world) / 1e9
     return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
-                call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=e2e_value, h2d=h2d, d2h=d2h,
-                launches=args.steps * (2 + (1 if splits > 1 else 0)))
+                call_reps=n_rep, call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=e2e_value,
+                h2d=h2d, d2h=d2h, launches=args.steps * (2 + (1 if splits > 1 else 0)), out=hout.clone())
 
 
 def decode_int8_leg(args, dev, code_dtype=torch.int8):
@@ -453,17 +463,18 @@ def decode_int8_leg(args, dev, code_dtype=torch.int8):
     stream = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    n_rep = max(args.steps, args.call_reps)
     start.record(stream)
-    for _ in range(args.steps):
+    for _ in range(n_rep):
         g.replay()
     end.record(stream)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / args.steps
+    ms = start.elapsed_time(end) / n_rep
     lens = case.seq_lens.tolist()
     positions = sum(int(L) for L in lens)
     nbytes = positions * Hkv * (2 * D * 1 + 2 * 4) + 2 * S * Hq * D * 2 + \
         sum(-(-int(L) // bs) for L in lens) * 4 + S * 4
-    return dict(ms=ms, bytes=nbytes, gbs=nbytes / (ms / 1e3) / 1e9)
+    return dict(ms=ms, bytes=nbytes, gbs=nbytes / (ms / 1e3) / 1e9, reps=n_rep)
 
 
 def cascade_leg(args, dev):
@@ -518,7 +529,7 @@ def cascade_leg(args, dev):
             fn()
         for _ in range(3):
             g.replay()
-        n = max(20, min(args.steps, 200))
+        n = max(50, args.config_calls)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         torch.cuda.synchronize()
         for i in range(n):
@@ -573,22 +584,26 @@ def prefill_leg(args, dev, steps):
     ql = (case.query_start_loc[1:] - case.query_start_loc[:-1]).tolist()
     flops = causal_flops(ql, case.seq_lens.tolist(), case.num_q_heads, case.head_dim)
     return dict(case=case, write_ms=write_ms, attn_ms=attn_ms, flops=flops, tflops=flops / (attn_ms / 1e3) / 1e12,
-                launches=2 * steps)
+                launches=2 * steps, out=out.cpu())
 
 
 def configs_leg(args, dev, peaks):
     """The other workloads of the hot path (the parity configurations): the fp32 latency case,
-    the ragged bf16 decode, the head_dim-256 decode and the mixed varlen batch. Each call is
-    captured in a CUDA graph and replayed; before every timed call 256 MB are rewritten and
+    the ragged bf16 decode, the head_dim-256 decode and the mixed varlen batch (on the default
+    grid, on a host-planned grid, and with its short requests on the split-KV decode). Each call
+    is captured in a CUDA graph and replayed; before every timed call 256 MB are rewritten and
     re-read so that no input stays in L2 (the fp32 case, whose 0.2 MB live in L2 between steps
     of a real decode loop, is also timed warm); CUDA events on the call's stream; median and
-    minimum of `n` calls. The two small decodes are also launched eagerly."""
+    minimum of `n` calls. The two small decodes are also launched eagerly. Returns the timings
+    and, per workload, the case, the GPU output of the timed call and how to run the oracle on
+    it (the parity check itself runs with the CPU baseline, outside every timed region)."""
     import paged_kv_attention_gb300 as pa
     import workloads
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     rd = torch.zeros(64 << 20, device=dev)
+    n_calls = max(50, args.config_calls)
 
-    def timed(fn, n=50, graph=True, cold=True):
+    def timed(fn, n=n_calls, graph=True, cold=True):
         for _ in range(5):
             fn()
         torch.cuda.synchronize()
@@ -615,7 +630,8 @@ def configs_leg(args, dev, peaks):
         return statistics.median(us), us[0]
 
     hbm, tf = peaks["hbm_gbs"], peaks["bf16_tflops"]
-    res = {}
+    res, outputs = {}, {}
+    launches = 0
     for name in ("decode_1seq_fp32", "decode_ragged32_bf16", "decode_64x4096_bf16_d256"):
         case = workloads.NAMED[name]()
         kc, vc = (t.to(dev) for t in case.empty_pools())
@@ -631,46 +647,83 @@ def configs_leg(args, dev, peaks):
             pa.paged_attention_decode(q, kc, vc, t, lens, case.scale, out=o, workspace=ws)
 
         med, mn = timed(call)
+        per_call = 2 if splits > 1 else 1
+        launches += n_calls * per_call
         elt = 4 if case.dtype == torch.float32 else 2
-        kv = sum(int(x) for x in case.seq_lens) * Hkv * D * elt * 2
-        entry = {"us_median": round(med, 2), "us_min": round(mn, 2), "splits": splits, "kv_bytes": kv,
-                 "queries_per_s": round(S / (med * 1e-6)),
-                 "GBps": round(kv / med / 1e3, 1), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
+        nbytes = decode_call_bytes(case.seq_lens.tolist(), Hq, Hkv, D, bs, elt)
+        entry = {"us_median": round(med, 2), "us_min": round(mn, 2), "splits": splits, "calls": n_calls,
+                 "algorithmic_bytes": nbytes, "queries_per_s": round(S / (med * 1e-6)),
+                 "GBps": round(nbytes / med / 1e3, 1), "frac_of_hbm_peak": round(nbytes / med / 1e3 / hbm, 4)}
         if name != "decode_64x4096_bf16_d256":
             emed, emn = timed(call, graph=False)
+            launches += n_calls * per_call
             entry["eager_us_median"], entry["eager_us_min"] = round(emed, 2), round(emn, 2)
         if name == "decode_1seq_fp32":
             wmed, wmn = timed(call, cold=False)
+            launches += n_calls * per_call
             entry["warm_us_median"], entry["warm_us_min"] = round(wmed, 2), round(wmn, 2)
+            ewmed, ewmn = timed(call, graph=False, cold=False)
+            launches += n_calls * per_call
+            entry["warm_eager_us_median"], entry["warm_eager_us_min"] = round(ewmed, 2), round(ewmn, 2)
+            entry.pop("GBps")
+            entry.pop("frac_of_hbm_peak")
+            entry["bound"] = "latency (0.2 MB: no bandwidth claim)"
         res[name] = entry
+        outputs[name] = (case, "decode", {}, o.cpu())
+        del kc, vc
     case = workloads.NAMED["varlen_mixed_bf16"]()
     kc, vc = (t.to(dev) for t in case.empty_pools())
     pa.reshape_and_cache(case.key.to(dev), case.value.to(dev), kc, vc, case.slot_mapping.to(dev))
     q = case.q.to(dev)
-    o = torch.empty_like(q)
     a = (kc, vc, case.query_start_loc.to(dev), case.seq_lens.to(dev), case.block_tables.to(dev), case.max_query_len,
          True, case.scale)
-    med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o))
     qls = (case.query_start_loc[1:] - case.query_start_loc[:-1]).tolist()
     sls = case.seq_lens.tolist()
-    pairs = sum(sum(min(L - ql + i + 1, L) for i in range(ql)) for ql, L in zip(qls, sls))
-    flops = 4 * case.head_dim * case.num_q_heads * pairs
-    kv = sum(sls) * case.num_kv_heads * case.head_dim * 2 * 2
-    res["varlen_mixed_bf16"] = {
-        "us_median": round(med, 2), "us_min": round(mn, 2), "causal_flops": flops, "kv_bytes": kv,
-        "queries_per_s": round(case.num_tokens / (med * 1e-6)),
-        "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
-        "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
-    # the same batch on a host-planned grid (pa_varlen_plan on the host copies of the lengths, the
-    # items copied to the device once; the plan itself is host work outside the timed call)
+    flops = causal_flops(qls, sls, case.num_q_heads, case.head_dim)
+    nbytes = sum(sls) * kv_bytes_per_token(case.num_kv_heads, case.head_dim, 2) + \
+        2 * case.num_tokens * case.num_q_heads * case.head_dim * 2
+    variants = [("varlen_mixed_bf16", dict(), "default grid: every tile pair up to max_query_len, heaviest first")]
     items = pa.varlen_plan(case.query_start_loc, case.seq_lens, case.max_query_len, case.num_q_heads,
                            case.num_kv_heads, True).to(dev)
-    med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o, work_items=items))
-    res["varlen_mixed_bf16_planned"] = {
-        "us_median": round(med, 2), "us_min": round(mn, 2), "items": int(items.numel()),
-        "queries_per_s": round(case.num_tokens / (med * 1e-6)),
-        "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(kv / med / 1e3, 1),
-        "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4), "frac_of_hbm_peak": round(kv / med / 1e3 / hbm, 4)}
+    variants.append(("varlen_mixed_bf16_planned", dict(work_items=items),
+                     "host-planned grid (pa_varlen_plan, outside the timed call): only the pairs the batch has"))
+    variants.append(("varlen_mixed_bf16_split_decodes", dict(split_decodes=True),
+                     "requests of <= 8 queries on the split-KV decode, the rest on the tensor-core kernel"))
+    for vname, kw, desc in variants:
+        o = torch.empty_like(q)
+        med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o, **kw))
+        launches += n_calls * (3 if kw.get("split_decodes") else 1)
+        res[vname] = {
+            "grid": desc, "us_median": round(med, 2), "us_min": round(mn, 2), "calls": n_calls,
+            "causal_flops": flops, "algorithmic_bytes": nbytes,
+            "queries_per_s": round(case.num_tokens / (med * 1e-6)),
+            "TFLOPs": round(flops / med / 1e6, 1), "GBps": round(nbytes / med / 1e3, 1),
+            "frac_of_tensor_peak": round(flops / med / 1e6 / tf, 4),
+            "frac_of_hbm_peak": round(nbytes / med / 1e3 / hbm, 4),
+            "floor_us": round(max(flops / tf / 1e6, nbytes / hbm / 1e3), 1)}
+        if "work_items" in kw:
+            res[vname]["items"] = int(items.numel())
+        outputs[vname] = (case, "varlen", {}, o.cpu())
+    return res, outputs, launches
+
+
+def config_parity(outputs):
+    """Max and mean |GPU - oracle| of each configuration's timed call (float64 oracle, every row;
+    run with the CPU baseline, outside every timed region)."""
+    import oracle
+    pools = {}
+    res = {}
+    for name, (case, kind, kw, got) in outputs.items():
+        if case.name not in pools:
+            pools[case.name] = oracle_pools(case)
+        ko, vo = pools[case.name]
+        if kind == "decode":
+            want = oracle.paged_attention_decode(case.q, ko, vo, case.block_tables, case.seq_lens, case.scale)
+        else:
+            want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, case.seq_lens,
+                                                 case.block_tables, True, case.scale)
+        d = (got.double() - want).abs()
+        res[name] = {"max_abs": float(d.max()), "mean_abs": float(d.mean()), "rows": int(got.shape[0])}
     return res
 
 
@@ -680,7 +733,13 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--prefill-steps", type=int, default=150,
+                    help="timed prefill calls (each 4 x 8192 call is ~1.6 ms)")
+    ap.add_argument("--call-reps", type=int, default=2000,
+                    help="replays behind each per-call time (decode call, 8-bit decodes)")
+    ap.add_argument("--config-calls", type=int, default=200,
+                    help="timed calls per parity configuration and for the cascade")
+    ap.add_argument("--no-configs", action="store_true", help="skip the parity-configuration legs")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "decode", "prefill", "int8", "cascade", "configs"], default="all",
@@ -706,7 +765,7 @@ def main():
     traffic = load_traffic()
 
     if args.only == "configs":
-        r = configs_leg(args, dev, peaks)
+        r, _, _ = configs_leg(args, dev, peaks)
         if rank == 0:
             print(json.dumps({"configs": r, "peak_source": peak_src, "l2": "256 MB rewritten and re-read before "
                               "every timed call"}), flush=True)
@@ -731,6 +790,7 @@ def main():
         q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
         f8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev, torch.float8_e4m3fn)
         cz = None if (args.no_cascade or args.only != "all") else cascade_leg(args, dev)
+        cf = None if (args.no_configs or args.only != "all") else configs_leg(args, dev, peaks)
     clk = clocks.summary()
     if d is None:
         if rank == 0 and p is not None:
@@ -809,6 +869,12 @@ def main():
             "max_abs_diff_vs_plain": cz["max_diff"],
             "l2": "256 MB rewritten, then 256 MB read, between timed calls",
             "gpu_launches": cz["launches"]}
+    if cf is not None:
+        line["configs"] = cf[0]
+        line["configs_note"] = ("parity configurations, each call a CUDA graph replay with 256 MB rewritten and "
+                                "re-read before it (L2 cold); median of the calls; gpu_launches counts their "
+                                "kernel launches")
+        line["configs_gpu_launches"] = cf[2]
     if rank == 0 and world == 1 and not args.no_cpu_baseline and case.num_reqs == 64:
         _, ko_vo = None, oracle_pools(case)
         v, dt, n, threads = time_oracle_decode(case, *ko_vo)
@@ -823,6 +889,29 @@ def main():
             torch.set_num_threads(threads)
         line["cpu_baseline"]["one_thread"] = {"value": round(v1, 4), "unit": "GB/s",
                                               "sample": f"{n1} sequences, {dt1:.1f} s"}
+        # parity of the timed calls against the same oracle, every row (outside every timed region)
+        import oracle
+        want = oracle.paged_attention_decode(case.q, *ko_vo, case.block_tables, case.seq_lens, case.scale)
+        diff = (d["out"].double() - want).abs()
+        parity = {case.name: {"max_abs": float(diff.max()), "mean_abs": float(diff.mean()),
+                              "rows": int(want.shape[0])}}
+        if cf is not None:
+            parity.update(config_parity(cf[1]))
+        if p is not None:
+            # the prefill: a sample of rows (the first and last 128 of every prompt and every 97th)
+            pc = p["case"]
+            qsl = pc.query_start_loc.tolist()
+            rows = sorted({t for r in range(pc.num_reqs) for t in
+                           list(range(qsl[r], qsl[r] + 128)) + list(range(qsl[r + 1] - 128, qsl[r + 1])) +
+                           list(range(qsl[r], qsl[r + 1], 97))})
+            idx = torch.tensor(rows)
+            pko, pvo = oracle_pools(pc)
+            want = oracle.paged_attention_varlen(pc.q, pko, pvo, pc.query_start_loc, pc.seq_lens, pc.block_tables,
+                                                 True, pc.scale, tokens=idx)
+            diff = (p["out"][idx].double() - want[idx]).abs()
+            parity[pc.name] = {"max_abs": float(diff.max()), "mean_abs": float(diff.mean()), "rows": len(rows),
+                               "rows_of": int(pc.num_tokens)}
+        line["parity_vs_oracle"] = parity
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,6 +1,8 @@
 """GPU parity of pa_paged_attention_varlen (prefill chunks, decodes and verify blocks in one
 flattened batch, causal by position) against the float64 oracle."""
 
+import functools
+
 import pytest
 import torch
 
@@ -40,21 +42,43 @@ def sample_tokens(case, stride=23, edge=40):
     return torch.tensor(sorted(picked))
 
 
-def test_mixed_batch():
+@functools.lru_cache(maxsize=1)
+def mixed_oracle_all_rows():
     case, (ko, vo) = named_case("varlen_mixed_bf16")
+    return oracle_varlen(case, ko, vo)
+
+
+@pytest.mark.parametrize("path", ["default", "split_decodes", "planned", "planned_split"])
+def test_mixed_batch_every_row(path):
+    """The mixed batch (8 prefill chunks of 512, 48 decodes, 8 verify blocks of 5: 4,184 rows x
+    32 heads), every element against the oracle, on each of the call's grids."""
+    case, _ = named_case("varlen_mixed_bf16")
     kc, vc = gpu_pools(case)
-    out = run_varlen(case, kc, vc)
-    rows = sample_tokens(case)
-    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), case.dtype, rows=rows, label="mixed")
+    split = path in ("split_decodes", "planned_split")
+    kw = dict(split_decodes=split)
+    if path.startswith("planned"):
+        items = pa.varlen_plan(case.query_start_loc, case.seq_lens, case.max_query_len, case.num_q_heads,
+                               case.num_kv_heads, case.causal, 0, split_decodes=split)
+        kw["work_items"] = items.to(DEV)
+    out = run_varlen(case, kc, vc, **kw)
+    check_close(out, mixed_oracle_all_rows(), case.dtype, label=f"mixed ({path})")
 
 
-def test_long_causal_prefill_sampled():
+def test_long_causal_prefill_one_whole_prompt():
+    """The 4 x 8192 causal prefill: one whole prompt (all 8,192 rows x 32 heads) against the oracle;
+    for the other three, every diagonal-tile row of their first and last tile pairs and a
+    stride-17 sample; every row of all four finite."""
     case, (ko, vo) = named_case("prefill_4x8192_bf16")
     kc, vc = gpu_pools(case)
     out = run_varlen(case, kc, vc)
-    rows = sample_tokens(case, stride=331, edge=150)
-    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), case.dtype, rows=rows, label="prefill 4x8192")
-    # a property every row must have, at full size: finite, and bounded by the values' range
+    qsl = case.query_start_loc.tolist()
+    whole = torch.arange(qsl[1], qsl[2])                      # request 1, all rows
+    check_close(out, oracle_varlen(case, ko, vo, tokens=whole), case.dtype, rows=whole,
+                label="prefill 4x8192, request 1 whole")
+    rows = sample_tokens(case, stride=17, edge=128)
+    rows = rows[(rows < qsl[1]) | (rows >= qsl[2])]
+    check_close(out, oracle_varlen(case, ko, vo, tokens=rows), case.dtype, rows=rows,
+                label="prefill 4x8192, other requests sampled")
     assert torch.isfinite(out.float()).all()
 
 
