@@ -548,11 +548,11 @@ def cascade_leg(args, dev):
                 max_diff=diff, launches=3 * n)
 
 
-def prefill_leg(args, dev, steps):
+def prefill_leg(args, dev, steps, workload=PREFILL_WORKLOAD):
     import paged_kv_attention_gb300 as pa
     import workloads
-    case = workloads.NAMED[PREFILL_WORKLOAD]()
-    if args.prefill_seqs != case.num_reqs:  # a smaller batch of the same workload (profiling)
+    case = workloads.NAMED[workload]()
+    if args.prefill_seqs != case.num_reqs and workload == PREFILL_WORKLOAD:  # a smaller batch of the same workload (profiling)
         case = workloads.make_case(f"prefill_{args.prefill_seqs}x8192_bf16", 1005, [8192] * args.prefill_seqs,
                                    [8192] * args.prefill_seqs, num_q_heads=32, num_kv_heads=8, head_dim=128,
                                    block_size=64, dtype=torch.bfloat16)
@@ -787,6 +787,8 @@ def main():
     with ClockSampler(local) as clocks:
         d = None if args.only == "prefill" else decode_leg(args, world, rank, dev)
         p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps)
+        p_dims = {} if (args.no_prefill or args.only != "all") else {
+            d: prefill_leg(args, dev, max(1, args.prefill_steps // 2), f"{PREFILL_WORKLOAD}_d{d}") for d in (256, 64)}
         q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
         f8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev, torch.float8_e4m3fn)
         cz = None if (args.no_cascade or args.only != "all") else cascade_leg(args, dev)
@@ -845,6 +847,14 @@ def main():
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": round(p["tflops"] / tf_peak, 4),
                          "peak_source": peak_src, "traffic": traffic.get("varlen_kernel")},
         }
+    for dim, pd in p_dims.items():
+        tf_peak = peaks["bf16_tflops"]
+        line[f"prefill_d{dim}"] = {
+            "workload": pd["case"].name + f" ({pd['case'].num_q_heads} q / {pd['case'].num_kv_heads} KV heads, "
+                                         f"head_dim {dim}, block 64, causal)",
+            "value": round(pd["tflops"], 2), "unit": "TFLOP/s", "attn_ms": round(pd["attn_ms"], 4),
+            "causal_flops": pd["flops"], "steps": max(1, args.prefill_steps // 2), "gpu_launches": pd["launches"],
+            "frac_of_tensor_peak": round(pd["tflops"] / tf_peak, 4), "peak_source": peak_src}
     if q8 is not None:
         line["decode_int8"] = {
             "workload": "decode_64x4096_int8 (same queries and tokens, int8 codes + fp32 scales)",
@@ -897,9 +907,11 @@ def main():
                               "rows": int(want.shape[0])}}
         if cf is not None:
             parity.update(config_parity(cf[1]))
-        if p is not None:
-            # the prefill: a sample of rows (the first and last 128 of every prompt and every 97th)
-            pc = p["case"]
+        for pp in [p] + list(p_dims.values()):
+            if pp is None:
+                continue
+            # a prefill: a sample of rows (the first and last 128 of every prompt and every 97th)
+            pc = pp["case"]
             qsl = pc.query_start_loc.tolist()
             rows = sorted({t for r in range(pc.num_reqs) for t in
                            list(range(qsl[r], qsl[r] + 128)) + list(range(qsl[r + 1] - 128, qsl[r + 1])) +
@@ -908,7 +920,7 @@ def main():
             pko, pvo = oracle_pools(pc)
             want = oracle.paged_attention_varlen(pc.q, pko, pvo, pc.query_start_loc, pc.seq_lens, pc.block_tables,
                                                  True, pc.scale, tokens=idx)
-            diff = (p["out"][idx].double() - want[idx]).abs()
+            diff = (pp["out"][idx].double() - want[idx]).abs()
             parity[pc.name] = {"max_abs": float(diff.max()), "mean_abs": float(diff.mean()), "rows": len(rows),
                                "rows_of": int(pc.num_tokens)}
         line["parity_vs_oracle"] = parity

@@ -202,9 +202,10 @@ pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const vo
  *   A request whose q_len exceeds its seq_len, or whose seq_len exceeds
  *   max_blocks_per_seq * block_size, gets zero rows and a flag.
  * Supported: D in {64, 128, 256}; bf16 with Hq/Hkv <= 16 and block_size % 16 == 0 (the
- *   tcgen05 tensor-core kernel serves D = 128, Hq/Hkv in {1,2,4,8,16}, block_size in
- *   {16,32,64,128}; other bf16 shapes run every query token as a one-split decode);
- *   f32 with (Hq/Hkv) * D <= 2048 and any block_size. */
+ *   tcgen05 tensor-core kernels serve every D with Hq/Hkv in {1,2,4,8,16} and block_size in
+ *   {16,32,64,128}: at D 64 and 128 a CTA's two query tiles share each K/V tile, at D 256 it
+ *   runs them one after the other; other bf16 shapes run every query token as a one-split
+ *   decode); f32 with (Hq/Hkv) * D <= 2048 and any block_size. */
 pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const void* v_cache,
                                     const int32_t* query_start_loc, const int32_t* seq_lens,
                                     const int32_t* block_tables,
@@ -390,7 +391,7 @@ size_t pa_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  *   prefix_len: DEVICE int32 scalar (so a captured graph follows a growing prefix); suffix_tables
  *   [S, max_blocks_per_seq]; suffix_lens [S] (may be 0). num_splits: suffix splits (0 = auto, at most 31).
  *   workspace: >= pa_cascade_workspace_bytes, 16-byte aligned, device memory; the caller owns it.
- *   Supported: head_dim 128, Hq/Hkv in {1,2,4,8,16}, block_size in {16,32,64,128}. */
+ *   Supported: head_dim 64 or 128, Hq/Hkv in {1,2,4,8,16}, block_size in {16,32,64,128}. */
 pa_status pa_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* prefix_table, const int32_t* prefix_len, int max_prefix_blocks,
                             const int32_t* suffix_tables, const int32_t* suffix_lens, int num_seqs,

@@ -647,6 +647,7 @@ extern "C" pa_status pa_paged_attention_varlen_planned(
     vp.num_q_heads = num_q_heads;
     vp.num_kv_heads = num_kv_heads;
     vp.group = G;
+    vp.head_dim = head_dim;
     vp.block_size = block_size;
     vp.num_blocks = num_blocks;
     vp.max_blocks = max_blocks_per_seq;
@@ -907,7 +908,7 @@ extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const
                                  block_size, num_blocks, max_blocks_per_seq, scale, PA_DTYPE_BF16);
   if (st != PA_OK) return st;
   const int G = num_q_heads / num_kv_heads;
-  if (!varlen_tc_supported(head_dim, G, block_size)) return PA_ERR_UNSUPPORTED;
+  if (!varlen_tc_prefix_supported(head_dim, G, block_size)) return PA_ERR_UNSUPPORTED;
   if ((long long)max_prefix_blocks * block_size > (1ll << 30)) return PA_ERR_UNSUPPORTED;
   if ((long long)num_seqs * num_kv_heads * kMaxSplits > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
   DeviceInfo* info = nullptr;
@@ -935,6 +936,7 @@ extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const
   vp.num_q_heads = num_q_heads;
   vp.num_kv_heads = num_kv_heads;
   vp.group = G;
+  vp.head_dim = head_dim;
   vp.block_size = block_size;
   vp.num_blocks = num_blocks;
   vp.max_blocks = max_prefix_blocks;

@@ -98,7 +98,8 @@ int decode_f32_ctas_per_sm(int head_dim, int group);
 // log-sum-exp merge of split partials into out.
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
 
-// tcgen05 varlen kernel (bf16, head_dim 128).
+// tcgen05 varlen kernels (bf16; head_dim 64 and 128: two query tiles per CTA sharing every K/V
+// tile; head_dim 256: the CTA's two query tiles one after the other).
 struct VarlenParams {
   const int32_t* query_start_loc;
   const int32_t* seq_lens;
@@ -110,6 +111,7 @@ struct VarlenParams {
   int num_q_heads;
   int num_kv_heads;
   int group;
+  int head_dim;
   int block_size;
   int num_blocks;
   int max_blocks;
@@ -143,8 +145,14 @@ struct VarlenParams {
   int num_items;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
+// the cascade's prefix pass (two query tiles per CTA): head_dim 64 and 128
+bool varlen_tc_prefix_supported(int head_dim, int group, int block_size);
+// query tokens one CTA (work item) covers: two 128-row tiles of 128 / group tokens, any head_dim
 int varlen_tc_tokens_per_cta(int group);
 cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream);
+// head_dim 256 (in varlen_tc256.cu); `ctas` already checked against the grid limit
+cudaError_t launch_varlen_tc256(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, long long ctas, cudaStream_t stream);
 
 }  // namespace pa

@@ -31,20 +31,16 @@
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "tc_common.cuh"
 
 namespace pa {
 namespace {
 
+using namespace tc;
+
 constexpr int kBM = 128;  // packed query rows per tile
-constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kD = 128;   // head dim of this kernel
 constexpr int kStages = 2;
-constexpr int kRegion = 128 * 128;       // one [128 rows][64 bf16] swizzled column half: 16 KiB
-constexpr int kTileBytes = 2 * kRegion;  // a 128 x 128 bf16 tile
-constexpr int kOffQ = 0;                 // Q_A, Q_B
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kRegion = 128 * 128;  // one [128 rows][64 bf16] swizzled 64-column block: 16 KiB
 enum {
   B_Q = 0,
   B_KF = 1,   // +stage
@@ -57,172 +53,36 @@ enum {
   B_FIN = 15,
   kNumBars = 16
 };
-constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 32;
+// Shared-memory layout for head dim kD (64 or 128): a tile of 128 rows is kD / 64 column blocks.
+template <int kD>
+struct Layout {
+  static constexpr int kTileBytes = (kD / 64) * kRegion;
+  static constexpr int kOffQ = 0;  // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 32;
+};
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns of tile t's score block and output accumulator
+// TMEM columns of tile t's score block and output accumulator (kD columns)
 __host__ __device__ constexpr uint32_t col_s(int t) { return t == 0 ? 0u : 128u; }
-__host__ __device__ constexpr uint32_t col_o(int t) { return t == 0 ? 256u : 384u; }
+template <int kD>
+__host__ __device__ constexpr uint32_t col_o(int t) { return t == 0 ? 256u : 256u + kD; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-
-// ---------------------------------------------------------------- tcgen05 helpers
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major, B K-major
-// or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-// Shared-memory matrix descriptor: start, leading and stride byte offsets (>> 4), the
-// sm_100 descriptor version (1 at bit 46) and the 128-byte swizzle mode (2 at bit 61).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// D(tmem) (+)= A(smem) * B(smem)
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// D(tmem) (+)= A(tmem) * B(smem); A is M rows on the TMEM lanes, two bf16 per column.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-#define PA_R32(v) \
-  "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), \
-  "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),       \
-  "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),      \
-  "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-#define PA_W32(v) \
-  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), \
-  "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),   \
-  "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),   \
-  "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-
-// 32 consecutive columns of this warp's 32 TMEM lanes (one row per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : PA_R32(v)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      PA_W32(v)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Bounded wait that also gives up as soon as another role has aborted. The clock and the
-// abort flag are checked once per 64 polls so that waiting warps take few issue slots.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// ---------------------------------------------------------------- softmax arithmetic
-// 2^x on the special-function unit (flushes results below 2^-126 to zero: such
-// probabilities are far below bf16 resolution against the row maximum's 1).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// Packed fp32 pairs (Blackwell f32x2 arithmetic: one instruction for two lanes of work).
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-// tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1): one ex2 and one approximate reciprocal; absolute
-// error ~1e-7 (the softcap multiplies it by the cap), exact limits +-1 at +-infinity.
-__device__ __forceinline__ float tanh_ex2(float y) {
-  const float e = ex2(y * 2.8853900817779268f);
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.f));
-  return 1.f - 2.f * r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// The same, with one verdict for the whole warp, so that a warp either proceeds to its
-// warp-collective tcgen05 instructions together or leaves together.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  const bool ok = wait_or_abort(bar, parity, abort_flag);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void set_abort(volatile int* abort_flag, int32_t* err) {
-  *abort_flag = 1;
-  flag_error(err, PA_ERRBIT_WAIT_TIMEOUT);
-}
-
-struct TileSpan {
-  int n_tok;    // valid query tokens in the tile (0 = tile unused)
-  int first;    // position of the tile's first query
-  int n_kv;     // 128-key tiles it needs
-};
-
-__device__ __forceinline__ TileSpan tile_span(int tok0, int TOK, int q_len, int seq_len, int causal) {
-  TileSpan t;
-  t.n_tok = max(0, min(TOK, q_len - tok0));
-  t.first = seq_len - q_len + tok0;
-  const int key_end = causal ? min(seq_len, t.first + t.n_tok) : seq_len;
-  t.n_kv = t.n_tok > 0 ? (key_end + kBN - 1) / kBN : 0;
-  return t;
-}
 
 // kPrefix: the cascade's shared-prefix pass (one request of num_tokens query rows that all
 // see the whole prefix; unnormalised partials out instead of normalised rows).
-template <bool kPrefix>
+template <bool kPrefix, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_tc_kernel(const __grid_constant__ VarlenParams p, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+  constexpr int kTileBytes = Layout<kD>::kTileBytes;
+  constexpr int kOffQ = Layout<kD>::kOffQ;
+  constexpr int kOffK = Layout<kD>::kOffK;
+  constexpr int kOffV = Layout<kD>::kOffV;
+  constexpr int kOffBar = Layout<kD>::kOffBar;
+  constexpr int kBlocks = kD / 64;  // 64-column blocks of a row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -369,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&vmap);
       mbar_arrive_expect_tx(&bars[B_Q], 2 * kTileBytes);
       for (int t = 0; t < 2; ++t)
-        for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < kBlocks; ++a)
           tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
                       q_start + tok0 + t * TOK);
     }
@@ -385,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t round_parity = ((i / kStages) - 1) & 1;
       const int p0 = (j0 + i) * pages_per_tile;
       const int np = min(p0 + pages_per_tile, seq_pages) - p0;
-      const uint32_t bytes = (uint32_t)np * bs * 256u;
+      const uint32_t bytes = (uint32_t)np * bs * (uint32_t)(kD * 2);
       const int nxt = i + 1 < n_kv ? page_of(i + 1) : 0;
       if (i >= kStages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
         if (lane == 0) set_abort(abort_flag, p.err);
@@ -395,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < np) {
         if (cur < 0 || cur >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
-        for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < kBlocks; ++a)
           tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st],
                       a * 64, kvh, 0, cur);
       }
@@ -409,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
       __syncwarp();
       if (lane < np)
-        for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < kBlocks; ++a)
           tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st],
                       a * 64, kvh, 0, cur);
       __syncwarp();
@@ -441,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars[B_SF + t]);
       }
     };
-    // O_t += P_t(j) V_j (N = 128: both 64-column halves of V), P_t from the first 64 TMEM
+    // O_t += P_t(j) V_j (N = kD: every 64-column block of V), P_t from the first 64 TMEM
     // columns of S block t
     auto issue_pv = [&](int t, int j) {
       if (lane == 0) {
@@ -449,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), id_pv,
+          umma_ts(tmem + col_o<kD>(t), tmem + col_s(t) + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), id_pv,
                   kk > 0 ? 1u : acc0);
         umma_commit(&bars[B_OD + t]);
       }
@@ -472,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (zero_from < kBN) {
         uint8_t* vbp = smem + kOffV + st * kTileBytes;
         const int rows = kBN - zero_from;
-        for (int i = lane; i < rows * 16; i += 32) {
-          const int row = zero_from + i / 16, c = i % 16;
+        for (int i = lane; i < rows * (kD / 8); i += 32) {
+          const int row = zero_from + i / (kD / 8), c = i % (kD / 8);
           *reinterpret_cast<uint4*>(vbp + (c >> 3) * kRegion + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();
@@ -519,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = p.scale_log2;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + col_s(t);
-    const uint32_t o_col = lane_base + col_o(t);
+    const uint32_t o_col = lane_base + col_o<kD>(t);
     // a sink logit starts the running state: it joins the denominator and adds no value
     float m_run = p.sinks != nullptr ? p.sinks[kvh * G + row % G] * kLog2e : -INFINITY;
     float l_run = p.sinks != nullptr ? 1.f : 0.f;
@@ -601,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? alpha : 1.f;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < kD / 32; ++q4) {
           uint32_t ov[32];
           tmem_ld32(o_col + 32 * q4, ov);
           tmem_ld_wait();
@@ -626,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n_mine > 0) {
         tc_fence_after();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < kD / 32; ++q4) {
           uint32_t ov[32];
           tmem_ld32(o_col + 32 * q4, ov);
           tmem_ld_wait();
@@ -647,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)(q_start + tok) * p.out_stride +
                            (size_t)(kvh * G + row % G) * kD;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < kD / 32; ++q4) {
         uint32_t ov[32];
         tmem_ld32(o_col + 32 * q4, ov);
         tmem_ld_wait();
@@ -695,33 +555,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool varlen_tc_supported(int head_dim, int group, int block_size) {
   const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8 || group == 16;
   const bool bs_ok = block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128;
-  return head_dim == kD && g_ok && bs_ok;
+  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && g_ok && bs_ok;
+}
+
+bool varlen_tc_prefix_supported(int head_dim, int group, int block_size) {
+  return head_dim != 256 && varlen_tc_supported(head_dim, group, block_size);
 }
 
 int varlen_tc_tokens_per_cta(int group) { return 2 * (kBM / group); }
 
+namespace {
+template <bool kPrefix, int kD>
+cudaError_t launch_pair(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                        const CUtensorMap& vmap, long long ctas, cudaStream_t stream) {
+  // the shared-memory opt-in is per device and kernel; setting it twice is harmless
+  static std::atomic<bool> attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  constexpr int smem = Layout<kD>::kSmemBytes;
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(varlen_tc_kernel<kPrefix, kD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
+  }
+  varlen_tc_kernel<kPrefix, kD><<<(unsigned)ctas, kThreads, smem, stream>>>(p, qmap, kmap, vmap);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_varlen_tc(const VarlenParams& p_in, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {
   VarlenParams p = p_in;
-  if (p.out_stride == 0) p.out_stride = (long long)p.num_q_heads * kD;  // dense rows
-  // the shared-memory opt-in is per device and kernel; setting it twice is harmless
-  static std::atomic<bool> attr_done[64][2] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int mode = p.prefix_mode ? 1 : 0;
-  auto kern = p.prefix_mode ? varlen_tc_kernel<true> : varlen_tc_kernel<false>;
-  if (dev < 0 || dev >= 64 || !attr_done[dev][mode].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev][mode].store(true, std::memory_order_release);
-  }
+  if (p.out_stride == 0) p.out_stride = (long long)p.num_q_heads * p.head_dim;  // dense rows
   const long long ctas = (p.work_items != nullptr && !p.prefix_mode ? (long long)p.num_items
                                                                      : (long long)p.q_tiles * p.num_reqs) *
                          p.num_kv_heads;
   if (ctas <= 0) return cudaSuccess;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(p, qmap, kmap, vmap);
-  return cudaGetLastError();
+  if (p.head_dim == 256) {
+    if (p.prefix_mode) return cudaErrorInvalidValue;
+    return launch_varlen_tc256(p, qmap, kmap, vmap, ctas, stream);
+  }
+  if (p.head_dim == 64)
+    return p.prefix_mode ? launch_pair<true, 64>(p, qmap, kmap, vmap, ctas, stream)
+                         : launch_pair<false, 64>(p, qmap, kmap, vmap, ctas, stream);
+  if (p.head_dim == 128)
+    return p.prefix_mode ? launch_pair<true, 128>(p, qmap, kmap, vmap, ctas, stream)
+                         : launch_pair<false, 128>(p, qmap, kmap, vmap, ctas, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -57,6 +57,21 @@ def test_prefix_lengths_and_groups(prefix_len, hq, hkv, bs):
         check_close(out, want, torch.bfloat16, label=f"P{prefix_len} G{hq // hkv} bs{bs} splits={splits}")
 
 
+@pytest.mark.parametrize("prefix_len", [0, 37, 1000])
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 1, 32), (8, 4, 64)])
+def test_head_dim_64(prefix_len, hq, hkv, bs):
+    """The prefix pass at head_dim 64 (one 64-column block per row), several suffix splits."""
+    suffix = [0, 1, 17, 200, 333, 64]
+    case = workloads.cascade_case("c64", 900 + prefix_len + hq + bs, prefix_len, suffix, num_q_heads=hq,
+                                  num_kv_heads=hkv, head_dim=64, block_size=bs, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    want = oracle_cascade(case, ko, vo)
+    for splits in (1, 0):
+        out = run_cascade(case, kc, vc, splits=splits)
+        check_close(out, want, torch.bfloat16, label=f"D64 P{prefix_len} G{hq // hkv} bs{bs} splits={splits}")
+
+
 @pytest.mark.parametrize("num_seqs", [1, 63, 64, 65, 130, 300])
 def test_many_sequences_span_query_tiles(num_seqs):
     """More sequences than one CTA's query rows (64 at G=4): several prefix tiles, ragged last."""
@@ -139,7 +154,7 @@ def test_workspace_too_small_and_unsupported_shapes():
     with pytest.raises(pa.PagedAttentionError) as e:
         run_cascade(case, kc, vc, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
     assert e.value.status == pa._lib.PA_ERR_WORKSPACE_TOO_SMALL
-    small = workloads.cascade_case("cu", 832, 300, [20, 30], num_q_heads=8, num_kv_heads=2, head_dim=64,
+    small = workloads.cascade_case("cu", 832, 300, [20, 30], num_q_heads=8, num_kv_heads=2, head_dim=256,
                                    block_size=16, dtype=torch.bfloat16)
     kc2, vc2 = gpu_pools(small)
     with pytest.raises(pa.PagedAttentionError) as e:

@@ -21,8 +21,8 @@ DEV = "cuda"
 LEVELS = [0.0, 10.0, 60.0, 0.0, 120.0, 125.0, -30.0, 126.0]
 
 
-def rising_case(seed, q_lens, seq_lens, hq, hkv, bs):
-    case = workloads.make_case("rise", seed, q_lens, seq_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+def rising_case(seed, q_lens, seq_lens, hq, hkv, bs, head_dim=128):
+    case = workloads.make_case("rise", seed, q_lens, seq_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=head_dim,
                                block_size=bs, dtype=torch.bfloat16)
     key = case.key.float()
     off = 0
@@ -57,6 +57,27 @@ def test_varlen_rising_scores(hq, hkv, bs, mod):
                                         case.scale, sinks=None if sinks is None else sinks.to(DEV),
                                         split_decodes=split, **kw)
         check_close(out, want, torch.bfloat16, label=f"rising varlen G{hq // hkv} bs{bs} {mod} split={split}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("head_dim,hq,hkv,bs", [(64, 32, 8, 16), (64, 16, 1, 64), (256, 16, 4, 64),
+                                                 (256, 8, 8, 16), (256, 16, 1, 32)])
+@pytest.mark.parametrize("mod", MODS, ids=lambda m: "-".join(f"{k}{v}" for k, v in m.items()) or "plain")
+def test_varlen_rising_scores_other_head_dims(head_dim, hq, hkv, bs, mod):
+    """The same jumps on the head_dim 64 and 256 tensor-core kernels (at 256 a rescale of O waits
+    for the previous tile's P.V, which may still be running when the next scores are ready)."""
+    q_lens, seq_lens = [700, 130, 1, 40], [700, 1000, 900, 600]
+    case = rising_case(1300 + head_dim + hq + bs, q_lens, seq_lens, hq, hkv, bs, head_dim)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    sinks = torch.full((hq,), mod["sinks"], dtype=torch.float32) if "sinks" in mod else None
+    kw = dict(window=mod.get("window", 0), softcap=mod.get("softcap", 0.0))
+    want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, case.seq_lens, case.block_tables,
+                                         True, case.scale, sinks=None if sinks is None else sinks.double(), **kw)
+    out = pa.paged_attention_varlen(case.q.to(DEV), kc, vc, case.query_start_loc.to(DEV), case.seq_lens.to(DEV),
+                                    case.block_tables.to(DEV), max(q_lens), True, case.scale,
+                                    sinks=None if sinks is None else sinks.to(DEV), **kw)
+    check_close(out, want, torch.bfloat16, label=f"rising varlen D{head_dim} G{hq // hkv} bs{bs} {mod}")
 
 
 @pytest.mark.gpu

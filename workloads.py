@@ -16,7 +16,8 @@ slot past a sequence's length shows it.
 Named workloads (sizes from the hot path's published shapes: 32 query / 8 KV
 heads of head_dim 128 is the Qwen3-8B attention shape the pages use):
   decode_1seq_fp32 / decode_ragged32_bf16 / decode_64x4096_bf16 (+ the
-  head_dim 256 variant) / varlen_mixed_bf16 / prefill_4x8192_bf16.
+  head_dim 256 variant) / varlen_mixed_bf16 / prefill_4x8192_bf16 (+ head_dim 256
+  and 64 variants).
 """
 
 from __future__ import annotations
@@ -192,11 +193,17 @@ def varlen_mixed_bf16() -> PagedCase:
                      gen=gen)
 
 
-def prefill_4x8192_bf16() -> PagedCase:
-    """4 prompts of 8192 tokens each, causal, block 64 (512 permuted pages),
-    32 q / 8 KV heads, head_dim 128, bf16."""
-    return make_case("prefill_4x8192_bf16", 1005, [8192] * 4, [8192] * 4, num_q_heads=32,
-                     num_kv_heads=8, head_dim=128, block_size=64, dtype=torch.bfloat16)
+def prefill_4x8192_bf16(head_dim: int = 128) -> PagedCase:
+    """4 prompts of 8192 tokens each, causal, block 64 (512 permuted pages), bf16.
+    head_dim 128: 32 q / 8 KV heads; head_dim 256: 16 q / 4 KV heads (the same causal flops);
+    head_dim 64: 32 q / 8 KV heads."""
+    if head_dim == 128:
+        return make_case("prefill_4x8192_bf16", 1005, [8192] * 4, [8192] * 4, num_q_heads=32,
+                         num_kv_heads=8, head_dim=128, block_size=64, dtype=torch.bfloat16)
+    hq, hkv = (16, 4) if head_dim == 256 else (32, 8)
+    return make_case(f"prefill_4x8192_bf16_d{head_dim}", 1015 if head_dim == 256 else 1016, [8192] * 4,
+                     [8192] * 4, num_q_heads=hq, num_kv_heads=hkv, head_dim=head_dim, block_size=64,
+                     dtype=torch.bfloat16)
 
 
 def cascade_case(name: str, seed: int, prefix_len: int, suffix_lens: list[int], **kw) -> PagedCase:
@@ -222,5 +229,7 @@ NAMED = {
     "decode_64x4096_bf16_d256": lambda: decode_64x4096_bf16(256),
     "varlen_mixed_bf16": varlen_mixed_bf16,
     "prefill_4x8192_bf16": prefill_4x8192_bf16,
+    "prefill_4x8192_bf16_d256": lambda: prefill_4x8192_bf16(256),
+    "prefill_4x8192_bf16_d64": lambda: prefill_4x8192_bf16(64),
     "cascade_64x4000_bf16": cascade_64x4000_bf16,
 }
