@@ -687,12 +687,23 @@ def configs_leg(args, dev, peaks):
                            case.num_kv_heads, True).to(dev)
     variants.append(("varlen_mixed_bf16_planned", dict(work_items=items),
                      "host-planned grid (pa_varlen_plan, outside the timed call): only the pairs the batch has"))
-    variants.append(("varlen_mixed_bf16_split_decodes", dict(split_decodes=True),
-                     "requests of <= 8 queries on the split-KV decode, the rest on the tensor-core kernel"))
+    ws = torch.empty(max(pa._lib.load().pa_varlen_workspace_bytes(case.num_reqs, case.num_q_heads, case.head_dim,
+                                                                   case.block_tables.shape[1], case.block_size), 16),
+                     dtype=torch.uint8, device=dev)
+    variants.append(("varlen_mixed_bf16_device_plan", dict(workspace=ws, schedule="tensor"),
+                     "grid planned on the device by a one-CTA kernel in the call (graph-safe), every request on "
+                     "the tensor-core kernel"))
+    variants.append(("varlen_mixed_bf16_split_decodes", dict(workspace=ws, schedule="split"),
+                     "device-planned grid; requests of <= 8 queries on the split-KV decode, launched to fill the "
+                     "tensor-core grid's tail"))
+    variants.append(("varlen_mixed_bf16_auto", dict(workspace=ws, schedule="auto"),
+                     "pa_paged_attention_varlen_ws: device-planned grid, short requests routed by the batch's "
+                     "shape (here: the tensor-core kernel)"))
     for vname, kw, desc in variants:
         o = torch.empty_like(q)
         med, mn = timed(lambda: pa.paged_attention_varlen(q, *a, out=o, **kw))
-        launches += n_calls * (3 if kw.get("split_decodes") else 1)
+        sched = kw.get("schedule")
+        launches += n_calls * (4 if sched == "split" else 2 if sched in ("tensor", "auto") else 1)
         res[vname] = {
             "grid": desc, "us_median": round(med, 2), "us_min": round(mn, 2), "calls": n_calls,
             "causal_flops": flops, "algorithmic_bytes": nbytes,

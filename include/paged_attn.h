@@ -277,15 +277,8 @@ pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const
                                        void* out, const pa_attn_options* options, int32_t* error_word,
                                        void* stream);
 
-/* pa_paged_attention_varlen_ex with a workspace. The same result; with a non-NULL workspace the
- * batch's short requests (1 to 8 queries: decodes and speculative verify blocks) are served by
- * the split-KV decode (its splits keep long contexts streaming at HBM speed; each query sees
- * its own causal range) and every other request by the tensor-core kernel ("TileInfer.jl -
- * Attention kernels", Decode: GQA packing and split-KV, the verify step); with NULL this is
- * pa_paged_attention_varlen_ex. workspace: device memory of
- * >= pa_varlen_workspace_bytes(...) bytes, 16-byte aligned, fully overwritten, not shared by
- * calls that overlap on the GPU; PA_ERR_WORKSPACE_TOO_SMALL when it is shorter. Two launches
- * (three with the decode's combine) on `stream`. */
+/* pa_paged_attention_varlen_ex with a workspace: pa_paged_attention_varlen_sched with
+ * PA_SHORT_AUTO (NULL workspace: pa_paged_attention_varlen_ex). */
 pa_status pa_paged_attention_varlen_ws(const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* query_start_loc, const int32_t* seq_lens,
                                        const int32_t* block_tables,
@@ -308,6 +301,50 @@ pa_status pa_paged_attention_varlen_strided(const void* q, const void* k_cache, 
                                             void* out, const pa_attn_options* options,
                                             const pa_row_strides* strides, void* workspace,
                                             size_t workspace_bytes, int32_t* error_word, void* stream);
+
+/* Where a varlen call with a workspace runs the batch's short requests (1 to 8 queries:
+ * decodes and speculative verify blocks). */
+typedef enum {
+  PA_SHORT_AUTO = 0,   /* the split-KV decode for a batch of many short requests (num_reqs >= 64
+                          and num_tokens <= 32 * num_reqs), else the tensor-core kernel (its decode
+                          tiles then run beside the prefill tiles from the start; the split path's
+                          extra launches only pay off over many short requests) */
+  PA_SHORT_SPLIT = 1,  /* always the split-KV decode */
+  PA_SHORT_TENSOR = 2  /* always the tensor-core kernel */
+} pa_short_requests;
+
+/* The varlen call on a grid planned on the device. The result is that of
+ * pa_paged_attention_varlen (within the bf16 tolerance; bit for bit with PA_SHORT_TENSOR).
+ * With a non-NULL workspace:
+ *   - a one-CTA plan kernel reads query_start_loc and seq_lens on the device when the call runs
+ *     and writes the batch's (tile pair, request) items, longest first by their key tiles, to the
+ *     front of the workspace ("TileInfer.jl - Attention kernels", Open questions: heaviest causal
+ *     blocks first); the tensor-core kernel, launched as its programmatic dependent, runs exactly
+ *     those items on a grid of min(num_reqs * cdiv(max_query_len, 256 / G), num_tokens / (256 / G)
+ *     + num_reqs) items x Hkv CTAs (the extra CTAs leave at once). Everything depends on host
+ *     sizes and device buffers only, so a captured CUDA graph follows lengths and query layouts
+ *     that change between replays;
+ *   - short requests on the split-KV decode (per short_requests) are served by it, launched after
+ *     the tensor-core grid as its programmatic dependent (its CTAs take the SMs that grid's tail
+ *     frees), then its combine ("TileInfer.jl - Attention kernels", Decode: GQA packing and
+ *     split-KV, the verify step; each query sees its own causal range).
+ *   workspace: device memory of >= pa_varlen_workspace_bytes(...) bytes, 16-byte aligned, fully
+ *   overwritten, not shared by calls that overlap on the GPU; PA_ERR_WORKSPACE_TOO_SMALL when
+ *   shorter. NULL workspace: the default grid with every request on the tensor-core kernel
+ *   (PA_SHORT_SPLIT then returns PA_ERR_WORKSPACE_TOO_SMALL). Up to four launches on `stream`.
+ *   Other arguments, layouts and errors: pa_paged_attention_varlen_strided. bf16 shapes the
+ *   tensor-core kernels serve; others run as pa_paged_attention_varlen (no workspace used). */
+pa_status pa_paged_attention_varlen_sched(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                                          const int32_t* block_tables,
+                                          int num_reqs, int num_tokens, int max_query_len,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, int max_blocks_per_seq,
+                                          int causal, float scale, pa_dtype dtype,
+                                          void* out, const pa_attn_options* options,
+                                          const pa_row_strides* strides, pa_short_requests short_requests,
+                                          void* workspace, size_t workspace_bytes, int32_t* error_word,
+                                          void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * Planned varlen grid. The tensor-core kernel's default grid is every (query tile pair,
@@ -336,7 +373,9 @@ int pa_varlen_plan(const int32_t* query_start_loc, const int32_t* seq_lens, int 
                    int32_t* work_items, int capacity);
 
 /* pa_paged_attention_varlen_strided on a planned grid: work_items is a DEVICE copy of
- * pa_varlen_plan's output (num_items entries; NULL = the default grid). The plan must come from
+ * pa_varlen_plan's output (num_items entries; NULL = pa_paged_attention_varlen_strided). With
+ * work_items and a non-NULL workspace the short requests go to the split-KV decode (make the plan
+ * with skip_upto 8), without a workspace to the tensor-core kernel. The plan must come from
  * the same batch: an item naming a tile past max_query_len is flagged (PA_ERRBIT_QUERY_LAYOUT)
  * and skipped, a request left out of the plan gets no rows. Same results as the default grid,
  * bit for bit (each pair's CTA computes the same thing, only the order changes). */
@@ -352,10 +391,11 @@ pa_status pa_paged_attention_varlen_planned(const void* q, const void* k_cache, 
                                             size_t workspace_bytes, const int32_t* work_items, int num_items,
                                             int32_t* error_word, void* stream);
 
-/* Workspace bytes pa_paged_attention_varlen_ws needs: the split partials of num_reqs short
- * requests (8 queries per request, at most 8 splits): num_reqs * 8 * min(8, chunks) * Hq *
- * (D + 2) * 4 with chunks = cdiv(max_blocks_per_seq * block_size, 16); 0 when one split covers
- * every context. Host only. */
+/* Workspace bytes pa_paged_attention_varlen_ws / _sched need: the device-planned work list,
+ * num_reqs * cdiv(max_blocks_per_seq * block_size, 16) int32 rounded up to 256 bytes, then the
+ * split partials of num_reqs short requests (8 queries per request, at most 8 splits):
+ * num_reqs * 8 * min(8, chunks) * Hq * (D + 2) * 4 with chunks = cdiv(max_blocks_per_seq *
+ * block_size, 16), none when one split covers every context. 0 for num_reqs <= 0. Host only. */
 size_t pa_varlen_workspace_bytes(int num_reqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
                                  int block_size);
 

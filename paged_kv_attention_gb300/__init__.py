@@ -209,13 +209,19 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            error_word: torch.Tensor | None = None,
                            stream: torch.cuda.Stream | None = None, window: int = 0, softcap: float = 0.0,
                            sinks: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                           split_decodes: bool = False, work_items: torch.Tensor | None = None) -> torch.Tensor:
+                           split_decodes: bool = False, work_items: torch.Tensor | None = None,
+                           schedule: str | None = None) -> torch.Tensor:
     """Flattened prefill / verify / decode batch; request r's queries are the newest q_len of
     its seq_lens[r] positions, causal by position. ``window``, ``softcap`` and ``sinks`` are
-    the pa_attn_options score modifiers. With ``split_decodes`` (bf16), the batch's short
-    requests (1 to 8 queries: decodes, verify blocks) go to the split-KV decode (a workspace is
-    allocated unless one is given): faster for batches of short requests, slower for
-    prefill-heavy ones (two launches in turn instead of one grid)."""
+    the pa_attn_options score modifiers.
+
+    ``schedule`` (pa_paged_attention_varlen_sched; a workspace is allocated unless one is given):
+    "auto", "split" or "tensor" run the tensor-core kernel on a grid planned on the device (only
+    the tile pairs the batch has, longest first; graph-safe), with the short requests (1 to 8
+    queries) on the split-KV decode for "split", on the tensor-core kernel for "tensor", and for
+    "auto" on the split-KV decode when the batch has >= 64 requests averaging <= 32 queries.
+    Without ``schedule``: ``work_items`` (a host plan, see varlen_plan) or the default grid, with
+    ``split_decodes`` sending the short requests to the split-KV decode."""
     n, hq, d = q.shape
     nb, bs, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     r = seq_lens.shape[0]
@@ -223,14 +229,27 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if out is None:
         out = torch.empty_like(q)
     lib = _lib.load()
-    if split_decodes and q.dtype == torch.bfloat16 and workspace is None:
+    modes = {"auto": _lib.PA_SHORT_AUTO, "split": _lib.PA_SHORT_SPLIT, "tensor": _lib.PA_SHORT_TENSOR}
+    if split_decodes and schedule is None and work_items is None:
+        schedule = "split"
+    if schedule is not None and schedule not in modes:
+        raise ValueError(f"schedule must be one of {sorted(modes)}")
+    if (split_decodes or schedule is not None) and q.dtype == torch.bfloat16 and workspace is None:
         workspace = torch.empty(max(int(lib.pa_varlen_workspace_bytes(r, hq, d, mb, bs)), 16), dtype=torch.uint8,
                                 device=q.device)
-    if not split_decodes:
+    if schedule is None and not split_decodes:
         workspace = None
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
     strides = _strides(q, out)
-    if work_items is not None:
+    if schedule is not None:
+        if work_items is not None:
+            raise ValueError("schedule plans on the device: pass no work_items")
+        st = lib.pa_paged_attention_varlen_sched(
+            _row_ptr(q)[0], _ptr(k_cache), _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+            _ptr(block_tables), r, n, int(max_query_len), hq, hkv, d, bs, nb, mb, int(bool(causal)),
+            float(scale or 0.0), _dtype(q), _row_ptr(out)[0], _options(window, softcap, sinks), strides,
+            modes[schedule], _ptr(workspace), ws_len, _ptr(error_word), _stream(stream))
+    elif work_items is not None:
         if work_items.dtype != torch.int32 or not work_items.is_cuda:
             raise ValueError("work_items must be an int32 CUDA tensor (varlen_plan's output, copied)")
         st = lib.pa_paged_attention_varlen_planned(

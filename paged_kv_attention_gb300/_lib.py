@@ -19,6 +19,10 @@ PA_DTYPE_BF16 = 1
 PA_DTYPE_INT8 = 2
 PA_DTYPE_FP8_E4M3 = 3
 
+PA_SHORT_AUTO = 0
+PA_SHORT_SPLIT = 1
+PA_SHORT_TENSOR = 2
+
 PA_ERRBIT_PAGE_OUT_OF_POOL = 1
 PA_ERRBIT_LENGTH_OUT_OF_RANGE = 2
 PA_ERRBIT_SLOT_OUT_OF_POOL = 4
@@ -84,6 +88,8 @@ SIGNATURES = {
     "pa_varlen_plan": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _i]),
     "pa_paged_attention_varlen_planned": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                                _i, _f, _i, _p, _opt, _rs, _p, _sz, _p, _i, _p, _p]),
+    "pa_paged_attention_varlen_sched": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                             _i, _f, _i, _p, _opt, _rs, _i, _p, _sz, _p, _p]),
 }
 
 _lib = None

@@ -359,7 +359,14 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
                     : -1;
   }
   const Unit u = resolve_unit(p, unit, threadIdx.x == 0 && split == 0 && kvh == 0);
-  if (u.skip) return;  // uniform: another kernel serves this unit
+  // Launched to overlap the previous kernel on the stream (which this one does not read): one CTA
+  // waits for that kernel's completion before it exits, so this grid completes only after it and
+  // a kernel that waits for this grid also sees the previous one's writes. (A no-op otherwise.)
+  const bool waits_for_previous = p.overlap_previous && blockIdx.x == 0 && blockIdx.y == 0;
+  if (u.skip) {  // uniform: another kernel serves this unit
+    if (waits_for_previous) asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
   const int n_chunks = (u.len + kChunk - 1) / kChunk;
   const int c_begin = max(split * p.chunks_per_split, u.start / kChunk);
   const int c_end = min(n_chunks, split * p.chunks_per_split + p.chunks_per_split);
@@ -788,9 +795,7 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
   }
   __syncthreads();
   merge_and_store<__nv_bfloat16>(p, merge_o, merge_ml, C::kConsumers, ROWS, D, unit, u, kvh, split);
-  // launched to overlap the previous kernel (which this one does not read): finish only after it
-  // (a no-op for an ordinary launch)
-  if (p.overlap_previous) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (waits_for_previous) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ fp32 CUDA-core decode

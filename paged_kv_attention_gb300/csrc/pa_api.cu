@@ -287,8 +287,45 @@ int auto_splits(DeviceInfo* info, int units, int Hkv, int D, int G, long long ma
   return (int)cdivll(max_chunks, per);
 }
 
+// Bytes at the front of a varlen workspace that hold the device-planned work list: room for
+// every tile pair the grid could index, num_reqs * cdiv(max_query_len, 16) (a CTA covers at least
+// 16 queries), rounded up to 256 bytes.
+size_t varlen_plan_bytes(int num_reqs, int max_query_len) {
+  const long long items = (long long)num_reqs * cdivll(std::max(max_query_len, 1), 16);
+  return (size_t)cdivll(items * 4, 256) * 256;
+}
+
+// Split count and partial layout of run_decode_units (without launching): the plan it will make.
+int decode_units_splits(const DecodeParams& p, pa_dtype dtype, int requested_splits, DeviceInfo* info);
+
 // Launch the decode-style kernels over `p.num_units` units (already filled in except the
 // split fields), then the combine when splitting.
+int decode_units_splits(const DecodeParams& p, pa_dtype dtype, int requested_splits, DeviceInfo* info) {
+  const long long max_chunks = cdivll((long long)p.max_blocks * p.block_size, kChunk);
+  const int T = std::max(1, p.unit_tokens);  // queries per unit; the kernel's rows are T * group
+  int splits = requested_splits;
+  if (splits <= 0)
+    splits = auto_splits(info, p.num_units, p.num_kv_heads, p.head_dim, p.group * T, max_chunks, dtype, p.quant);
+  if (p.varlen == 2) splits = std::min(splits, kShortRequestMaxSplits);
+  splits = (int)std::min<long long>(splits, max_chunks);
+  const int per = (int)cdivll(max_chunks, splits);
+  return (int)cdivll(max_chunks, per);
+}
+
+// The workspace check of run_decode_units (auto splits), done before the varlen call launches
+// anything: a refused call must enqueue nothing.
+pa_status check_decode_units_workspace(const DecodeParams& p, const void* workspace, size_t workspace_bytes) {
+  DeviceInfo* info = nullptr;
+  if (!device_info(&info)) return PA_ERR_CUDA;
+  const int splits = decode_units_splits(p, PA_DTYPE_BF16, 0, info);
+  if (splits <= 1) return PA_OK;
+  const size_t need = (size_t)p.num_units * splits * std::max(1, p.unit_tokens) * p.num_q_heads *
+                      ((size_t)p.head_dim + 2) * 4;
+  if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return PA_ERR_INVALID_ARGUMENT;
+  return PA_OK;
+}
+
 pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache, const void* v_cache,
                            int requested_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   DeviceInfo* info = nullptr;
@@ -296,13 +333,8 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   const int D = p.head_dim;
   const long long max_chunks = cdivll((long long)p.max_blocks * p.block_size, kChunk);
   const int T = std::max(1, p.unit_tokens);  // queries per unit; the kernel's rows are T * group
-  int splits = requested_splits;
-  if (splits <= 0)
-    splits = auto_splits(info, p.num_units, p.num_kv_heads, D, p.group * T, max_chunks, dtype, p.quant);
-  if (p.varlen == 2) splits = std::min(splits, kShortRequestMaxSplits);
-  splits = (int)std::min<long long>(splits, max_chunks);
+  const int splits = decode_units_splits(p, dtype, requested_splits, info);
   const int per = (int)cdivll(max_chunks, splits);
-  splits = (int)cdivll(max_chunks, per);
   p.num_splits = splits;
   p.chunks_per_split = per;
   p.slot_count = splits;
@@ -474,8 +506,12 @@ extern "C" size_t pa_varlen_workspace_bytes(int num_reqs, int num_q_heads, int h
   if (num_reqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0) return 0;
   const long long max_chunks = cdivll((long long)max_blocks_per_seq * block_size, kChunk);
   const long long splits = std::min<long long>(kShortRequestMaxSplits, max_chunks);
-  if (splits <= 1) return 0;
-  return (size_t)((long long)num_reqs * kShortRequestQueries * splits * num_q_heads * ((long long)head_dim + 2) * 4);
+  // the device-planned work list first (a query length never exceeds the table's capacity)
+  const long long max_q = std::min<long long>((long long)max_blocks_per_seq * block_size, 1ll << 30);
+  const size_t plan = varlen_plan_bytes(num_reqs, (int)max_q);
+  if (splits <= 1) return plan;
+  return plan +
+         (size_t)((long long)num_reqs * kShortRequestQueries * splits * num_q_heads * ((long long)head_dim + 2) * 4);
 }
 
 extern "C" pa_status pa_paged_attention_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -574,12 +610,27 @@ extern "C" int pa_varlen_plan(const int32_t* query_start_loc, const int32_t* seq
   return (int)items.size();
 }
 
-extern "C" pa_status pa_paged_attention_varlen_planned(
-    const void* q, const void* k_cache, const void* v_cache, const int32_t* query_start_loc, const int32_t* seq_lens,
-    const int32_t* block_tables, int num_reqs, int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
-    int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
-    void* out, const pa_attn_options* options, const pa_row_strides* strides, void* workspace, size_t workspace_bytes,
-    const int32_t* work_items, int num_items, int32_t* error_word, void* stream) {
+namespace pa {
+namespace {
+// PA_SHORT_AUTO sends the short requests to the split-KV decode when the batch has at least
+// kAutoSplitMinReqs requests averaging at most kAutoSplitMaxAvgQueries queries. The split path adds
+// a launch chain (plan, tensor-core grid, decode, combine: ~10 us) that only many short requests
+// repay, while on the tensor-core grid decode tiles run beside the prefill tiles from the start.
+// Measured on GB300 (us, planned tensor-core grid vs split, L2 cold): 8 prefill chunks of 512 + 48
+// decodes + 8 verify blocks 186 vs 205; 48 decodes + 8 verify blocks 111 vs 119; 2 chunks + 48
+// decodes + 8 verify 136 vs 146; 48 decodes 99 vs 99; 1 chunk + 64 decodes 121 vs 118; 4 chunks +
+// 128 decodes 260 vs 254; 256 decodes 420 vs 358.
+constexpr int kAutoSplitMinReqs = 64;
+constexpr int kAutoSplitMaxAvgQueries = 32;
+
+pa_status varlen_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                      const int32_t* seq_lens, const int32_t* block_tables, int num_reqs, int num_tokens,
+                      int max_query_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, int max_blocks_per_seq, int causal, float scale, pa_dtype dtype, void* out,
+                      const pa_attn_options* options, const pa_row_strides* strides, int short_requests,
+                      void* workspace, size_t workspace_bytes, const int32_t* work_items, int num_items,
+                      int32_t* error_word, void* stream) {
+  if (short_requests < PA_SHORT_AUTO || short_requests > PA_SHORT_TENSOR) return PA_ERR_INVALID_ARGUMENT;
   if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
   if (work_items != nullptr && num_items < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_reqs == 0 || num_tokens == 0) return PA_OK;
@@ -598,10 +649,78 @@ extern "C" pa_status pa_paged_attention_varlen_planned(
     // With a workspace, the short requests of the batch (decodes, verify blocks of up to
     // kShortRequestQueries queries) go to the split-KV decode, whose splits keep long contexts
     // streaming at HBM speed; a 128-row tensor-core tile would carry only their few rows, in one
-    // CTA per request and KV head. The tensor-core kernel takes every other request.
-    const bool split_decodes = workspace != nullptr;
+    // CTA per request and KV head. The tensor-core kernel takes every other request, on a grid
+    // planned on the device (only the tile pairs the batch has, longest first) unless the caller
+    // passes a host plan. Launch order: the plan, the tensor-core grid, then the split-KV decode
+    // as a programmatic dependent whose CTAs fill the SMs the tensor-core grid's tail leaves
+    // free, and its combine.
+    // a host plan: the short requests are on the split path iff there is a workspace (the plan
+    // was made with the matching skip); otherwise the schedule decides, and a workspace carries
+    // the device-planned work list
+    if (workspace == nullptr && short_requests == PA_SHORT_SPLIT && work_items == nullptr)
+      return PA_ERR_WORKSPACE_TOO_SMALL;
+    const bool split_decodes =
+        work_items != nullptr
+            ? workspace != nullptr
+            : workspace != nullptr &&
+                  (short_requests == PA_SHORT_SPLIT ||
+                   (short_requests == PA_SHORT_AUTO && num_reqs >= kAutoSplitMinReqs &&
+                    (long long)num_tokens <= (long long)kAutoSplitMaxAvgQueries * num_reqs));
+    const int skip_upto = split_decodes ? kShortRequestQueries : 0;
+    const int q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
+    int32_t* plan_items = nullptr;
+    int plan_capacity = 0;
+    if (workspace != nullptr && work_items == nullptr) {
+      const long long cap = varlen_device_plan_capacity(num_reqs, num_tokens, max_query_len, G, skip_upto);
+      const size_t plan_bytes = varlen_plan_bytes(num_reqs, max_query_len);
+      if ((size_t)cap * 4 > plan_bytes || workspace_bytes < plan_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+      if (!aligned16(workspace)) return PA_ERR_INVALID_ARGUMENT;
+      plan_items = static_cast<int32_t*>(workspace);
+      plan_capacity = (int)cap;
+      workspace = static_cast<uint8_t*>(workspace) + plan_bytes;
+      workspace_bytes -= plan_bytes;
+    }
+    VarlenParams vp{};
+    vp.skip_upto = skip_upto;
+    vp.query_start_loc = query_start_loc;
+    vp.seq_lens = seq_lens;
+    vp.block_tables = block_tables;
+    vp.out = out;
+    vp.err = error_word;
+    vp.num_reqs = num_reqs;
+    vp.num_tokens = num_tokens;
+    vp.num_q_heads = num_q_heads;
+    vp.num_kv_heads = num_kv_heads;
+    vp.group = G;
+    vp.head_dim = head_dim;
+    vp.block_size = block_size;
+    vp.num_blocks = num_blocks;
+    vp.max_blocks = max_blocks_per_seq;
+    vp.max_query_len = max_query_len;
+    vp.out_stride = out_stride;
+    if (plan_items != nullptr) {
+      vp.work_items = plan_items;
+      vp.num_items = plan_capacity;
+      vp.plan_on_device = 1;
+    } else {
+      vp.work_items = work_items;
+      vp.num_items = work_items != nullptr ? num_items : 0;
+    }
+    const int tokens_per_tile = 128 / G;
+    vp.q_tiles = q_tiles;
+    vp.causal = causal ? 1 : 0;
+    vp.scale_log2 = sc * kLog2e;
+    st = apply_options(options, sc, vp);
+    if (st != PA_OK) return st;
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile, q_stride) ||
+        !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks,
+                          block_size < 128 ? block_size : 128) ||
+        !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks,
+                          block_size < 128 ? block_size : 128))
+      return PA_ERR_CUDA;
+    DecodeParams dp{};
     if (split_decodes) {
-      DecodeParams dp{};
       dp.q = q;
       dp.k_cache = k_cache;
       dp.v_cache = v_cache;
@@ -630,45 +749,19 @@ extern "C" pa_status pa_paged_attention_varlen_planned(
       dp.q_stride = q_stride;
       dp.out_stride = out_stride;
       dp.scale_log2 = sc * kLog2e;
+      dp.overlap_previous = 1;
       st = apply_options(options, sc, dp);
       if (st != PA_OK) return st;
-      st = run_decode_units(dp, PA_DTYPE_BF16, k_cache, v_cache, 0, workspace, workspace_bytes, s);
+      st = check_decode_units_workspace(dp, workspace, workspace_bytes);
       if (st != PA_OK) return st;
     }
-    VarlenParams vp{};
-    vp.skip_upto = split_decodes ? kShortRequestQueries : 0;
-    vp.query_start_loc = query_start_loc;
-    vp.seq_lens = seq_lens;
-    vp.block_tables = block_tables;
-    vp.out = out;
-    vp.err = error_word;
-    vp.num_reqs = num_reqs;
-    vp.num_tokens = num_tokens;
-    vp.num_q_heads = num_q_heads;
-    vp.num_kv_heads = num_kv_heads;
-    vp.group = G;
-    vp.head_dim = head_dim;
-    vp.block_size = block_size;
-    vp.num_blocks = num_blocks;
-    vp.max_blocks = max_blocks_per_seq;
-    vp.max_query_len = max_query_len;
-    vp.out_stride = out_stride;
-    vp.work_items = work_items;
-    vp.num_items = work_items != nullptr ? num_items : 0;
-    const int tokens_per_tile = 128 / G;
-    vp.q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
-    vp.causal = causal ? 1 : 0;
-    vp.scale_log2 = sc * kLog2e;
-    st = apply_options(options, sc, vp);
-    if (st != PA_OK) return st;
-    CUtensorMap qmap, kmap, vmap;
-    if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile, q_stride) ||
-        !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks,
-                          block_size < 128 ? block_size : 128) ||
-        !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks,
-                          block_size < 128 ? block_size : 128))
+    if (plan_items != nullptr &&
+        launch_varlen_device_plan(query_start_loc, seq_lens, num_reqs, num_tokens, G, q_tiles, causal ? 1 : 0,
+                                  vp.window, skip_upto, plan_items, plan_capacity, error_word, s) != cudaSuccess)
       return PA_ERR_CUDA;
-    return launch_varlen_tc(vp, qmap, kmap, vmap, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (launch_varlen_tc(vp, qmap, kmap, vmap, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (split_decodes) return run_decode_units(dp, PA_DTYPE_BF16, k_cache, v_cache, 0, workspace, workspace_bytes, s);
+    return PA_OK;
   }
 
   // Generic path: every query token is a decode over the keys it sees (one split).
@@ -698,6 +791,32 @@ extern "C" pa_status pa_paged_attention_varlen_planned(
   st = apply_options(options, sc, p);
   if (st != PA_OK) return st;
   return run_decode_units(p, dtype, k_cache, v_cache, 1, nullptr, 0, s);
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_paged_attention_varlen_planned(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* block_tables, int num_reqs, int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
+    void* out, const pa_attn_options* options, const pa_row_strides* strides, void* workspace, size_t workspace_bytes,
+    const int32_t* work_items, int num_items, int32_t* error_word, void* stream) {
+  return varlen_impl(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, num_reqs, num_tokens,
+                     max_query_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                     causal, scale, dtype, out, options, strides, PA_SHORT_AUTO, workspace, workspace_bytes,
+                     work_items, num_items, error_word, stream);
+}
+
+extern "C" pa_status pa_paged_attention_varlen_sched(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* block_tables, int num_reqs, int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int causal, float scale, pa_dtype dtype,
+    void* out, const pa_attn_options* options, const pa_row_strides* strides, pa_short_requests short_requests,
+    void* workspace, size_t workspace_bytes, int32_t* error_word, void* stream) {
+  return varlen_impl(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, num_reqs, num_tokens,
+                     max_query_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                     causal, scale, dtype, out, options, strides, (int)short_requests, workspace, workspace_bytes,
+                     nullptr, 0, error_word, stream);
 }
 
 // ------------------------------------------------------------------------------ 8-bit caches

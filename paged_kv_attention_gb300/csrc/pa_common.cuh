@@ -146,4 +146,24 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
   return row * 128u + ((unit ^ (row & 7u)) << 4);
 }
 
+// ---------------------------------------------------------------- launches
+// Launch `kern` as a programmatic dependent of the kernel before it on `stream`: its CTAs may
+// start once every CTA of that kernel has signalled (griddepcontrol.launch_dependents) or exited;
+// the kernel itself orders its reads with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 }  // namespace pa

@@ -140,9 +140,13 @@ struct VarlenParams {
   // is carried by the query tensor map.
   long long out_stride;
   // planned grid: CTA i serves item work_items[i / num_kv_heads] = tile * num_reqs + request
-  // (nullptr: every tile of every request, heaviest tile index first)
+  // (nullptr: every tile of every request, heaviest tile index first); a negative item is
+  // padding and its CTAs leave at once
   const int32_t* work_items;
   int num_items;
+  // 1: work_items is written by the plan kernel launched just before on the stream; this grid is
+  // launched as its programmatic dependent and waits for it before reading the list
+  int plan_on_device;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
 // the cascade's prefix pass (two query tiles per CTA): head_dim 64 and 128
@@ -151,6 +155,13 @@ bool varlen_tc_prefix_supported(int head_dim, int group, int block_size);
 int varlen_tc_tokens_per_cta(int group);
 cudaError_t launch_varlen_tc(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream);
+// Items the device-planned grid may hold for a batch of num_tokens queries in num_reqs requests
+// (requests of at most skip_upto queries are left to the split-KV decode): the grid's size.
+long long varlen_device_plan_capacity(int num_reqs, int num_tokens, int max_query_len, int group, int skip_upto);
+// The device-side work list: `capacity` int32 entries of `items`, longest item first, -1 padded.
+cudaError_t launch_varlen_device_plan(const int32_t* query_start_loc, const int32_t* seq_lens, int num_reqs,
+                                      int num_tokens, int group, int q_tiles, int causal, int window, int skip_upto,
+                                      int32_t* items, int capacity, int32_t* err, cudaStream_t stream);
 // head_dim 256 (in varlen_tc256.cu); `ctas` already checked against the grid limit
 cudaError_t launch_varlen_tc256(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, long long ctas, cudaStream_t stream);

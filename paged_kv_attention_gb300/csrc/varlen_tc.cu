@@ -94,11 +94,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pairs), else heaviest (last) query tiles first across all requests and heads
   int tile, r, kvh;  // r: the request, or the prefix key range in prefix mode
   if (!kPrefix && p.work_items != nullptr) {
-    const int item = __ldg(p.work_items + blockIdx.x / p.num_kv_heads);
+    // a list planned on the device by the kernel launched just before this one: wait for it
+    if (p.plan_on_device) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int item = p.plan_on_device ? p.work_items[blockIdx.x / p.num_kv_heads]
+                                      : __ldg(p.work_items + blockIdx.x / p.num_kv_heads);
     kvh = (int)(blockIdx.x % p.num_kv_heads);
+    if (item < 0) return;  // padding past the plan's last item
     tile = item / p.num_reqs;
     r = item - tile * p.num_reqs;
-    if (item < 0 || tile >= p.q_tiles) {  // not an item of this batch: nothing to do here
+    if (tile >= p.q_tiles) {  // not an item of this batch: nothing to do here
       if (threadIdx.x == 0 && kvh == 0) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
       return;
     }
@@ -565,6 +569,121 @@ bool varlen_tc_prefix_supported(int head_dim, int group, int block_size) {
 int varlen_tc_tokens_per_cta(int group) { return 2 * (kBM / group); }
 
 namespace {
+
+// ---------------------------------------------------------------- device-side work list
+// The planned grid's work list, built on the GPU from the batch's lengths as they are when the
+// call runs (so a captured graph follows them): every (tile pair, request) item the batch has,
+// longest first by its key-tile count ("TileInfer.jl - Attention kernels", Open questions:
+// heaviest causal blocks first), then -1 up to the grid's capacity. One CTA: a histogram of the
+// items' key-tile counts, a descending scan, and a scatter (the order among items of equal
+// count is not fixed; each item computes the same result wherever it runs).
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 4096;  // counts of 4095 key tiles and more share the last bucket
+
+struct PlanArgs {
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  int32_t* items;
+  int32_t* err;
+  int num_reqs;
+  int num_tokens;
+  int tok_tile;  // tokens of one 128-row query tile (128 / group)
+  int q_tiles;   // tile pairs per request in the grid's index space
+  int causal;
+  int window;
+  int skip_upto;
+  int capacity;
+};
+
+// Key tiles of pair t of request r (its larger tile's count), or -1 if the pair is no item: the
+// request is empty, served by the split-KV decode, or has fewer queries.
+__device__ int plan_pair_work(const PlanArgs& a, int r, int t) {
+  const int start = a.query_start_loc[r], stop = a.query_start_loc[r + 1];
+  const int q_len = stop - start;
+  if (q_len <= 0) return -1;
+  if (start >= 0 && stop <= a.num_tokens && q_len <= a.skip_upto) return -1;
+  const int tok0 = t * 2 * a.tok_tile;
+  if (tok0 >= q_len) return -1;
+  const int seq = a.seq_lens[r];
+  int w = 0;
+  for (int h = 0; h < 2; ++h) {
+    const int t0 = tok0 + h * a.tok_tile;
+    const int n = max(0, min(a.tok_tile, q_len - t0));
+    if (n == 0) continue;
+    const int first = seq - q_len + t0;
+    const int key_end = a.causal ? min(seq, first + n) : seq;
+    const int j0 = a.window > 0 ? max(0, first - a.window + 1) / 128 : 0;
+    w = max(w, (max(0, key_end) + 127) / 128 - j0);
+  }
+  return max(0, w);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const __grid_constant__ PlanArgs a) {
+  __shared__ int start[kPlanBuckets];
+  __shared__ int warp_sums[kPlanThreads / 32];
+  __shared__ int total;
+  // the tensor-core grid launched after this kernel may start now; it waits for this grid's
+  // completion before it reads the list
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x;
+  for (int b = tid; b < kPlanBuckets; b += kPlanThreads) start[b] = 0;
+  __syncthreads();
+  const long long pairs = (long long)a.num_reqs * a.q_tiles;
+  for (long long i = tid; i < pairs; i += kPlanThreads) {
+    const int r = (int)(i / a.q_tiles), t = (int)(i % a.q_tiles);
+    const int w = plan_pair_work(a, r, t);
+    if (w >= 0) atomicAdd(&start[min(w, kPlanBuckets - 1)], 1);
+  }
+  __syncthreads();
+  // exclusive scan over the buckets in descending order: thread k owns buckets
+  // kPlanBuckets - 1 - 4k - c (c = 0..3); start[b] becomes the first slot of bucket b
+  constexpr int kPer = kPlanBuckets / kPlanThreads;
+  int cnt[kPer], run = 0;
+#pragma unroll
+  for (int c = 0; c < kPer; ++c) {
+    cnt[c] = start[kPlanBuckets - 1 - (tid * kPer + c)];
+    run += cnt[c];
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += v;
+    }
+    warp_sums[lane] = ws;  // inclusive over warps
+    if (lane == 31) total = ws;
+  }
+  __syncthreads();
+  int off = incl - run + (warp > 0 ? warp_sums[warp - 1] : 0);
+#pragma unroll
+  for (int c = 0; c < kPer; ++c) {
+    start[kPlanBuckets - 1 - (tid * kPer + c)] = off;
+    off += cnt[c];
+  }
+  __syncthreads();
+  for (long long i = tid; i < pairs; i += kPlanThreads) {
+    const int r = (int)(i / a.q_tiles), t = (int)(i % a.q_tiles);
+    const int w = plan_pair_work(a, r, t);
+    if (w < 0) continue;
+    const int pos = atomicAdd(&start[min(w, kPlanBuckets - 1)], 1);
+    if (pos < a.capacity)
+      a.items[pos] = t * a.num_reqs + r;
+    else
+      flag_error(a.err, PA_ERRBIT_QUERY_LAYOUT);  // more items than the grid's bound: a malformed layout
+  }
+  for (int i = total + tid; i < a.capacity; i += kPlanThreads) a.items[i] = -1;
+}
+
 template <bool kPrefix, int kD>
 cudaError_t launch_pair(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                         const CUtensorMap& vmap, long long ctas, cudaStream_t stream) {
@@ -579,10 +698,45 @@ cudaError_t launch_pair(const VarlenParams& p, const CUtensorMap& qmap, const CU
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
-  varlen_tc_kernel<kPrefix, kD><<<(unsigned)ctas, kThreads, smem, stream>>>(p, qmap, kmap, vmap);
-  return cudaGetLastError();
+  if (!p.plan_on_device) {
+    varlen_tc_kernel<kPrefix, kD><<<(unsigned)ctas, kThreads, smem, stream>>>(p, qmap, kmap, vmap);
+    return cudaGetLastError();
+  }
+  return launch_dependent(varlen_tc_kernel<kPrefix, kD>, (unsigned)ctas, kThreads, smem, stream, p, qmap, kmap,
+                          vmap);
 }
 }  // namespace
+
+long long varlen_device_plan_capacity(int num_reqs, int num_tokens, int max_query_len, int group, int skip_upto) {
+  const int per_cta = varlen_tc_tokens_per_cta(group);
+  const long long q_tiles = (max_query_len + per_cta - 1) / per_cta;
+  // a request with q queries has cdiv(q, per_cta) <= q / per_cta + 1 pairs; the queries of the
+  // requests add up to num_tokens, and with short requests skipped a planned request has more
+  // than skip_upto queries
+  const long long planned_reqs =
+      std::min<long long>(num_reqs, skip_upto > 0 ? num_tokens / (skip_upto + 1) : num_reqs);
+  return std::min<long long>((long long)num_reqs * q_tiles, num_tokens / per_cta + planned_reqs);
+}
+
+cudaError_t launch_varlen_device_plan(const int32_t* query_start_loc, const int32_t* seq_lens, int num_reqs,
+                                      int num_tokens, int group, int q_tiles, int causal, int window, int skip_upto,
+                                      int32_t* items, int capacity, int32_t* err, cudaStream_t stream) {
+  PlanArgs a;
+  a.query_start_loc = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.items = items;
+  a.err = err;
+  a.num_reqs = num_reqs;
+  a.num_tokens = num_tokens;
+  a.tok_tile = kBM / group;
+  a.q_tiles = q_tiles;
+  a.causal = causal;
+  a.window = window;
+  a.skip_upto = skip_upto;
+  a.capacity = capacity;
+  varlen_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_varlen_tc(const VarlenParams& p_in, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {

@@ -105,11 +105,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- which tile pair: from the caller's plan, else heaviest (last) tile pairs first
   int tile, r, kvh;
   if (p.work_items != nullptr) {
-    const int item = __ldg(p.work_items + blockIdx.x / p.num_kv_heads);
+    // a list planned on the device by the kernel launched just before this one: wait for it
+    if (p.plan_on_device) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int item = p.plan_on_device ? p.work_items[blockIdx.x / p.num_kv_heads]
+                                      : __ldg(p.work_items + blockIdx.x / p.num_kv_heads);
     kvh = (int)(blockIdx.x % p.num_kv_heads);
+    if (item < 0) return;  // padding past the plan's last item
     tile = item / p.num_reqs;
     r = item - tile * p.num_reqs;
-    if (item < 0 || tile >= p.q_tiles) {
+    if (tile >= p.q_tiles) {
       if (threadIdx.x == 0 && kvh == 0) flag_error(p.err, PA_ERRBIT_QUERY_LAYOUT);
       return;
     }
@@ -517,8 +521,11 @@ cudaError_t launch_varlen_tc256(const VarlenParams& p, const CUtensorMap& qmap, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
-  varlen_tc256_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(p, qmap, kmap, vmap);
-  return cudaGetLastError();
+  if (!p.plan_on_device) {
+    varlen_tc256_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(p, qmap, kmap, vmap);
+    return cudaGetLastError();
+  }
+  return launch_dependent(varlen_tc256_kernel, (unsigned)ctas, kThreads, kSmemBytes, stream, p, qmap, kmap, vmap);
 }
 
 }  // namespace pa

@@ -114,10 +114,14 @@ def test_workspace_bytes(lib):
 
 def test_varlen_workspace_bytes(lib):
     f = lib.pa_varlen_workspace_bytes
-    # short requests: 8 query rows each, at most 8 splits (never more than the 16-token chunks)
-    assert f(64, 32, 128, 256, 16) == 64 * 8 * 8 * 32 * 130 * 4
-    assert f(4, 8, 64, 2, 16) == 4 * 8 * 2 * 8 * 66 * 4          # 2 chunks: at most 2 splits
-    assert f(4, 8, 64, 1, 16) == 0                                # one chunk: one split, no partials
+
+    def plan(reqs, max_q):  # the device-planned work list: reqs * cdiv(max_q, 16) int32, 256-byte rounded
+        return -(-(reqs * -(-max_q // 16) * 4) // 256) * 256
+    # then the short requests' partials: 8 query rows each, at most 8 splits (never more than the
+    # 16-token chunks)
+    assert f(64, 32, 128, 256, 16) == plan(64, 4096) + 64 * 8 * 8 * 32 * 130 * 4
+    assert f(4, 8, 64, 2, 16) == plan(4, 32) + 4 * 8 * 2 * 8 * 66 * 4     # 2 chunks: at most 2 splits
+    assert f(4, 8, 64, 1, 16) == plan(4, 16)                            # one chunk: one split, no partials
     assert f(0, 8, 64, 16, 16) == 0
 
 

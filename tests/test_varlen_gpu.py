@@ -333,3 +333,101 @@ def test_one_query_request_without_its_position_is_flagged():
     assert torch.equal(out[:1].float(), torch.zeros_like(out[:1].float()))
     ko, vo = oracle_pools(case)
     check_close(out[1:], oracle_varlen(case, ko, vo)[1:], torch.bfloat16, label="clean request")
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 4, 64), (16, 1, 32)])
+def test_device_planned_grid_follows_the_batch_under_graph_replay(hq, hkv, bs):
+    """With a workspace the tensor-core grid is planned on the device from the lengths as they
+    are when the call runs: a captured call replays correctly after both seq_lens and the query
+    layout (query_start_loc, same total) change, prefill chunks turning into decodes and back."""
+    layouts = [([300, 1, 5, 60, 1, 200], [900, 3000, 1100, 60, 17, 2500]),
+               ([1, 1, 500, 5, 60, 0], [40, 2600, 1500, 1200, 300, 10]),
+               ([8, 9, 1, 230, 318, 1], [8, 700, 2999, 230, 1400, 64])]
+    N = sum(layouts[0][0])
+    assert all(sum(q) == N for q, _ in layouts)
+    max_q = 512
+    width = 3000 // bs + 1
+    pool = max(sum(-(-x // bs) for x in L) for _, L in layouts) + 8   # one pool size for every layout
+    cases = [workloads.make_case("vdp", 3100 + i + hq + bs, q, L, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                                 block_size=bs, dtype=torch.bfloat16, pool_blocks=pool, table_multiple=width)
+             for i, (q, L) in enumerate(layouts)]
+    # one pool per layout, one set of device buffers the graph reads
+    q = torch.empty((N, hq, 128), dtype=torch.bfloat16, device=DEV)
+    qsl = torch.empty(len(layouts[0][0]) + 1, dtype=torch.int32, device=DEV)
+    lens = torch.empty(len(layouts[0][0]), dtype=torch.int32, device=DEV)
+    tables = torch.empty((len(layouts[0][0]), cases[0].block_tables.shape[1]), dtype=torch.int32, device=DEV)
+    pools = [gpu_pools(c) for c in cases]
+    kc = torch.empty_like(pools[0][0])
+    vc = torch.empty_like(pools[0][1])
+    out = torch.empty_like(q)
+    ws = torch.empty(max(pa._lib.load().pa_varlen_workspace_bytes(len(lens), hq, 128, tables.shape[1], bs), 16),
+                     dtype=torch.uint8, device=DEV)
+
+    def load(i):
+        c = cases[i]
+        q.copy_(c.q.to(DEV))
+        qsl.copy_(c.query_start_loc.to(DEV))
+        lens.copy_(c.seq_lens.to(DEV))
+        tables.copy_(c.block_tables.to(DEV))
+        kc.copy_(pools[i][0])
+        vc.copy_(pools[i][1])
+
+    def call():
+        pa.paged_attention_varlen(q, kc, vc, qsl, lens, tables, max_q, True, cases[0].scale, out=out, workspace=ws,
+                                  split_decodes=True)
+
+    load(0)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for i in (1, 2, 0):
+        load(i)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ko, vo = oracle_pools(cases[i])
+        check_close(out, oracle_varlen(cases[i], ko, vo), torch.bfloat16, label=f"device plan replay layout {i}")
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 2, 64)])
+def test_schedules(hq, hkv, bs):
+    """pa_paged_attention_varlen_sched: "tensor" (device-planned grid, every request on the tensor
+    cores) equals the default grid bit for bit; "split" equals the split path; "auto" picks the
+    split-KV decode for a batch of many short requests (>= 64 requests, <= 32 queries each on
+    average) and the tensor-core kernel otherwise; all agree with the oracle."""
+    heavy = workloads.make_case("vsch", 3200 + hq + bs, [300, 1, 5, 130, 1, 64], [900, 3000, 1100, 130, 17, 2500],
+                                num_q_heads=hq, num_kv_heads=hkv, head_dim=128, block_size=bs, dtype=torch.bfloat16)
+    gen = torch.Generator().manual_seed(3300 + hq + bs)
+    lq = [1, 5, 2, 1, 8, 3] * 11 + [100]
+    ls = [int(x) for x in torch.randint(120, 1500, (len(lq),), generator=gen)]
+    light = workloads.make_case("vsch", 3300 + hq + bs, lq, ls, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                                block_size=bs, dtype=torch.bfloat16)
+    assert heavy.num_reqs < 64 and light.num_reqs >= 64 and light.num_tokens <= 32 * light.num_reqs
+    for case in (heavy, light):
+        kc, vc = gpu_pools(case)
+        ko, vo = oracle_pools(case)
+        grid = run_varlen(case, kc, vc)
+        tensor = run_varlen(case, kc, vc, schedule="tensor")
+        split = run_varlen(case, kc, vc, schedule="split")
+        auto = run_varlen(case, kc, vc, schedule="auto")
+        assert torch.equal(grid, tensor)
+        assert torch.equal(auto, split if case is light else tensor)
+        want = oracle_varlen(case, ko, vo)
+        check_close(tensor, want, torch.bfloat16, label="tensor schedule")
+        check_close(split, want, torch.bfloat16, label="split schedule")
+
+
+def test_split_schedule_without_workspace_is_refused():
+    case = workloads.make_case("vschw", 3400, [3, 1], [10, 20], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    lib = pa._lib.load()
+    out = torch.empty_like(case.q.to(DEV))
+    st = lib.pa_paged_attention_varlen_sched(
+        case.q.to(DEV).data_ptr(), kc.data_ptr(), vc.data_ptr(), case.query_start_loc.to(DEV).data_ptr(),
+        case.seq_lens.to(DEV).data_ptr(), case.block_tables.to(DEV).data_ptr(), 2, 4, 3, 8, 2, 128, 16,
+        case.num_blocks, case.block_tables.shape[1], 1, 0.0, pa._lib.PA_DTYPE_BF16, out.data_ptr(), None, None,
+        pa._lib.PA_SHORT_SPLIT, None, 0, None, None)
+    assert st == pa._lib.PA_ERR_WORKSPACE_TOO_SMALL
