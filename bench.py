@@ -104,11 +104,11 @@ def load_traffic():
 
 
 def source_hash(source: str) -> str:
-    """Hash of one kernel source file plus the shared device header it includes."""
+    """Hash of one kernel source file plus the shared device headers it includes."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_gb300", "csrc")
-    for name in (source, "pa_common.cuh"):
+    for name in (source, "pa_common.cuh", "tc_common.cuh", "pa_internal.h"):
         try:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
@@ -757,6 +757,8 @@ def main():
                     help="run one leg only (profiling runs); 'configs' times the parity configurations")
     ap.add_argument("--decode-seqs", type=int, default=64, help="sequences of 4096 tokens in the decode leg")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prompts of 8192 tokens in the prefill leg")
+    ap.add_argument("--prefill-dim", type=int, choices=[64, 128, 256], default=128,
+                    help="head_dim of the prefill leg run by --only prefill (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the decode step eagerly, not as CUDA graphs")
     ap.add_argument("--no-int8", action="store_true", help="skip the 8-bit-cache decode legs (int8, fp8 E4M3)")
@@ -797,7 +799,8 @@ def main():
         return
     with ClockSampler(local) as clocks:
         d = None if args.only == "prefill" else decode_leg(args, world, rank, dev)
-        p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps)
+        pre_wl = PREFILL_WORKLOAD if args.prefill_dim == 128 else f"{PREFILL_WORKLOAD}_d{args.prefill_dim}"
+        p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps, pre_wl)
         p_dims = {} if (args.no_prefill or args.only != "all") else {
             d: prefill_leg(args, dev, max(1, args.prefill_steps // 2), f"{PREFILL_WORKLOAD}_d{d}") for d in (256, 64)}
         q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
@@ -865,7 +868,8 @@ def main():
                                          f"head_dim {dim}, block 64, causal)",
             "value": round(pd["tflops"], 2), "unit": "TFLOP/s", "attn_ms": round(pd["attn_ms"], 4),
             "causal_flops": pd["flops"], "steps": max(1, args.prefill_steps // 2), "gpu_launches": pd["launches"],
-            "frac_of_tensor_peak": round(pd["tflops"] / tf_peak, 4), "peak_source": peak_src}
+            "frac_of_tensor_peak": round(pd["tflops"] / tf_peak, 4), "peak_source": peak_src,
+            "traffic": traffic.get("varlen_tc256_kernel") if dim == 256 else None}
     if q8 is not None:
         line["decode_int8"] = {
             "workload": "decode_64x4096_int8 (same queries and tokens, int8 codes + fp32 scales)",
