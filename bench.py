@@ -108,7 +108,7 @@ def source_hash(source: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_gb300", "csrc")
-    for name in (source, "pa_common.cuh", "tc_common.cuh", "pa_internal.h"):
+    for name in (source, "pa_common.cuh", "tc_common.cuh"):
         try:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
@@ -548,7 +548,7 @@ def cascade_leg(args, dev):
                 max_diff=diff, launches=3 * n)
 
 
-def prefill_leg(args, dev, steps, workload=PREFILL_WORKLOAD):
+def prefill_leg(args, dev, steps, workload=PREFILL_WORKLOAD, code_dtype=None):
     import paged_kv_attention_gb300 as pa
     import workloads
     case = workloads.NAMED[workload]()
@@ -562,10 +562,28 @@ def prefill_leg(args, dev, steps, workload=PREFILL_WORKLOAD):
     qsl, sl, tables = case.query_start_loc.to(dev), case.seq_lens.to(dev), case.block_tables.to(dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
+    if code_dtype is not None:  # an 8-bit cache (codes + one fp32 scale per slot and KV head)
+        kc = torch.empty(kc.shape, dtype=code_dtype, device=dev)
+        vc = torch.empty(vc.shape, dtype=code_dtype, device=dev)
+        ks = torch.empty(kc.shape[:3], dtype=torch.float32, device=dev)
+        vs = torch.empty(kc.shape[:3], dtype=torch.float32, device=dev)
+
+        def write():
+            pa.reshape_and_cache_quant(key, value, kc, vc, ks, vs, slots)
+
+        def attend():
+            pa.paged_attention_varlen_quant(q, kc, vc, ks, vs, qsl, sl, tables, case.max_query_len, True,
+                                            case.scale, out=out)
+    else:
+        def write():
+            pa.reshape_and_cache(key, value, kc, vc, slots)
+
+        def attend():
+            pa.paged_attention_varlen(q, kc, vc, qsl, sl, tables, case.max_query_len, True, case.scale, out=out)
 
     def step():
-        pa.reshape_and_cache(key, value, kc, vc, slots)
-        pa.paged_attention_varlen(q, kc, vc, qsl, sl, tables, case.max_query_len, True, case.scale, out=out)
+        write()
+        attend()
 
     for _ in range(max(2, min(args.warmup, 3))):
         step()
@@ -574,9 +592,9 @@ def prefill_leg(args, dev, steps, workload=PREFILL_WORKLOAD):
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
         ev[i][0].record(stream)
-        pa.reshape_and_cache(key, value, kc, vc, slots)
+        write()
         ev[i][1].record(stream)
-        pa.paged_attention_varlen(q, kc, vc, qsl, sl, tables, case.max_query_len, True, case.scale, out=out)
+        attend()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
@@ -803,6 +821,8 @@ def main():
         p = None if (args.no_prefill or args.only == "decode") else prefill_leg(args, dev, args.prefill_steps, pre_wl)
         p_dims = {} if (args.no_prefill or args.only != "all") else {
             d: prefill_leg(args, dev, max(1, args.prefill_steps // 2), f"{PREFILL_WORKLOAD}_d{d}") for d in (256, 64)}
+        p_q8 = None if (args.no_prefill or args.no_int8 or args.only != "all") else \
+            prefill_leg(args, dev, max(1, args.prefill_steps // 2), code_dtype=torch.int8)
         q8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev)
         f8 = None if (args.no_int8 or args.only != "all") else decode_int8_leg(args, dev, torch.float8_e4m3fn)
         cz = None if (args.no_cascade or args.only != "all") else cascade_leg(args, dev)
@@ -870,6 +890,14 @@ def main():
             "causal_flops": pd["flops"], "steps": max(1, args.prefill_steps // 2), "gpu_launches": pd["launches"],
             "frac_of_tensor_peak": round(pd["tflops"] / tf_peak, 4), "peak_source": peak_src,
             "traffic": traffic.get("varlen_tc256_kernel") if dim == 256 else None}
+    if p_q8 is not None:
+        line["prefill_int8"] = {
+            "workload": "prefill_4x8192_int8 (the 4 x 8192 prompts over an int8 cache: codes + fp32 scales, "
+                        "dequantised to bf16 tiles in shared memory)",
+            "value": round(p_q8["tflops"], 2), "unit": "TFLOP/s", "attn_ms": round(p_q8["attn_ms"], 4),
+            "causal_flops": p_q8["flops"], "steps": max(1, args.prefill_steps // 2),
+            "gpu_launches": p_q8["launches"], "frac_of_tensor_peak": round(p_q8["tflops"] / peaks["bf16_tflops"], 4),
+            "peak_source": peak_src}
     if q8 is not None:
         line["decode_int8"] = {
             "workload": "decode_64x4096_int8 (same queries and tokens, int8 codes + fp32 scales)",
@@ -938,6 +966,19 @@ def main():
             diff = (pp["out"][idx].double() - want[idx]).abs()
             parity[pc.name] = {"max_abs": float(diff.max()), "mean_abs": float(diff.mean()), "rows": len(rows),
                                "rows_of": int(pc.num_tokens)}
+        if p_q8 is not None:
+            # the int8-cache prefill against the oracle over the oracle's own quantised cache, same rows
+            from oracle import quant
+            pc = p_q8["case"]
+            shape = (pc.num_blocks, pc.block_size, pc.num_kv_heads, pc.head_dim)
+            ko8, vo8 = torch.zeros(shape, dtype=torch.int8), torch.zeros(shape, dtype=torch.int8)
+            kso, vso = torch.zeros(shape[:3]), torch.zeros(shape[:3])
+            quant.reshape_and_cache_quant(pc.key, pc.value, ko8, vo8, kso, vso, pc.slot_mapping, "int8")
+            want = quant.paged_attention_varlen_quant(pc.q, ko8, vo8, kso, vso, pc.query_start_loc, pc.seq_lens,
+                                                      pc.block_tables, True, pc.scale, tokens=idx)
+            diff = (p_q8["out"][idx].double() - want[idx]).abs()
+            parity["prefill_4x8192_int8"] = {"max_abs": float(diff.max()), "mean_abs": float(diff.mean()),
+                                             "rows": len(rows), "rows_of": int(pc.num_tokens)}
         line["parity_vs_oracle"] = parity
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -476,9 +476,12 @@ pa_status pa_paged_attention_decode_quant(const void* q, const void* k_cache, co
                                           size_t workspace_bytes, const pa_attn_options* options,
                                           int32_t* error_word, void* stream);
 
-/* Varlen over an 8-bit cache: as pa_paged_attention_varlen_ex (q and out bf16); every query
- * token runs as a one-split decode over the keys it sees (correct at any size; the tensor-core
- * varlen kernel reads bf16 caches only). Supported shapes as pa_paged_attention_decode_quant. */
+/* Varlen over an 8-bit cache: as pa_paged_attention_varlen_ex (q and out bf16). At head_dim 128
+ * with Hq/Hkv in {1,2,4,8,16} and block_size in {16,32,64,128} it runs on the tensor-core kernel:
+ * each K / V tile's codes land in shared memory and are dequantised there to bf16 (code * scale,
+ * rounded once to fp32 and then to bf16: "32. Production attention kernels", Quantized KV caches)
+ * before the MMAs read them. Other shapes (head_dim 256) run every query token as a one-split
+ * decode over the codes. Supported shapes as pa_paged_attention_decode_quant. */
 pa_status pa_paged_attention_varlen_quant(const void* q, const void* k_cache, const void* v_cache,
                                           const float* k_scales, const float* v_scales, pa_dtype cache_dtype,
                                           const int32_t* query_start_loc, const int32_t* seq_lens,

@@ -924,6 +924,44 @@ extern "C" pa_status pa_paged_attention_varlen_quant(const void* q, const void* 
                                 num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
   if (st != PA_OK) return st;
   if ((long long)num_tokens * num_kv_heads > (1ll << 31) - 1) return PA_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+  if (head_dim == 128 && varlen_tc_supported(head_dim, G, block_size) && max_query_len > 0) {
+    // the tensor-core kernel: each K / V tile's codes are dequantised to bf16 in shared memory
+    // ("32. Production attention kernels", Quantized KV caches), then used like a bf16 tile
+    VarlenParams vp{};
+    vp.query_start_loc = query_start_loc;
+    vp.seq_lens = seq_lens;
+    vp.block_tables = block_tables;
+    vp.out = out;
+    vp.err = error_word;
+    vp.num_reqs = num_reqs;
+    vp.num_tokens = num_tokens;
+    vp.num_q_heads = num_q_heads;
+    vp.num_kv_heads = num_kv_heads;
+    vp.group = G;
+    vp.head_dim = head_dim;
+    vp.block_size = block_size;
+    vp.num_blocks = num_blocks;
+    vp.max_blocks = max_blocks_per_seq;
+    vp.max_query_len = max_query_len;
+    vp.q_tiles = (int)cdivll(max_query_len, varlen_tc_tokens_per_cta(G));
+    vp.causal = causal ? 1 : 0;
+    vp.scale_log2 = sc * kLog2e;
+    vp.quant = quant_kind(cache_dtype);
+    vp.k_scales = k_scales;
+    vp.v_scales = v_scales;
+    st = apply_options(options, sc, vp);
+    if (st != PA_OK) return st;
+    CUtensorMap qmap, kmap, vmap;
+    const int box = block_size < 128 ? block_size : 128;
+    if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, 128 / G,
+                          (long long)num_q_heads * head_dim) ||
+        !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, box, 1) ||
+        !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, box, 1))
+      return PA_ERR_CUDA;
+    return launch_varlen_tc(vp, qmap, kmap, vmap, as_stream(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   DecodeParams p{};
   p.q = q;
   p.k_cache = k_cache;
@@ -947,7 +985,6 @@ extern "C" pa_status pa_paged_attention_varlen_quant(const void* q, const void* 
   p.quant = quant_kind(cache_dtype);
   p.k_scales = k_scales;
   p.v_scales = v_scales;
-  const float sc = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
   p.scale_log2 = sc * kLog2e;
   st = apply_options(options, sc, p);
   if (st != PA_OK) return st;

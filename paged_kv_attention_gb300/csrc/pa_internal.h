@@ -147,6 +147,11 @@ struct VarlenParams {
   // 1: work_items is written by the plan kernel launched just before on the stream; this grid is
   // launched as its programmatic dependent and waits for it before reading the list
   int plan_on_device;
+  // 8-bit caches (head_dim 128): 0 = bf16, 1 = int8 codes, 2 = fp8 E4M3 codes; one fp32 scale per
+  // (slot, KV head) in k_scales / v_scales [blocks, bs, Hkv]
+  int quant;
+  const float* k_scales;
+  const float* v_scales;
 };
 bool varlen_tc_supported(int head_dim, int group, int block_size);
 // the cascade's prefix pass (two query tiles per CTA): head_dim 64 and 128

@@ -27,6 +27,8 @@
 //    reference max; this only bounds the range of P and O);
 //  * every wait is bounded; on expiry the CTA flags PA_ERRBIT_WAIT_TIMEOUT, drains its
 //    outstanding copies and MMAs, frees its tensor memory and exits.
+#include <cuda_fp16.h>
+
 #include <atomic>
 
 #include "pa_common.cuh"
@@ -51,19 +53,25 @@ enum {
   B_PR = 11,  // +tile
   B_OD = 13,  // +tile
   B_FIN = 15,
-  kNumBars = 16
+  B_KR = 16,  // +stage: 8-bit caches, the K tile is dequantised to bf16 (64 converter arrivals)
+  B_VR = 18,  // +stage: the same for V
+  kNumBars = 20
 };
 // Shared-memory layout for head dim kD (64 or 128): a tile of 128 rows is kD / 64 column blocks.
-template <int kD>
+// kQ (8-bit caches: 1 int8, 2 fp8 E4M3): a stage's codes land in its second column block and
+// are dequantised in place; its 128 key and 128 value scales sit after the V ring.
+template <int kD, int kQ = 0>
 struct Layout {
   static constexpr int kTileBytes = (kD / 64) * kRegion;
   static constexpr int kOffQ = 0;  // Q_A, Q_B
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffScale = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffScale + (kQ != 0 ? kStages * 256 * 4 : 0);
   static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 32;
 };
 constexpr int kThreads = 320;
+constexpr int kThreadsQ = 384;  // 8-bit caches: two more warps dequantise the K / V tiles
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of tile t's score block and output accumulator (kD columns)
 __host__ __device__ constexpr uint32_t col_s(int t) { return t == 0 ? 0u : 128u; }
@@ -71,17 +79,94 @@ template <int kD>
 __host__ __device__ constexpr uint32_t col_o(int t) { return t == 0 ? 256u : 256u + kD; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// ---------------------------------------------------------------- 8-bit cache tiles
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// Four int8 codes (one word) times the row's scale -> two bf16 pairs (dims in byte order). A
+// code c becomes exactly c as a float through the bits 0x4B0000xx (2^23 + the byte of c + 128)
+// minus 2^23 + 128; the product with the fp32 scale is rounded once to fp32, then to bf16.
+__device__ __forceinline__ void int8x4_to_bf16(uint32_t w, uint64_t s2, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint64_t bias = f2(-8388736.f, -8388736.f);
+  float a0, a1, a2, a3;
+  f2_split(f2_mul(f2_add(f2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)),
+                            __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541))),
+                         bias),
+                  s2),
+           a0, a1);
+  f2_split(f2_mul(f2_add(f2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542)),
+                            __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543))),
+                         bias),
+                  s2),
+           a2, a3);
+  lo = pack_bf16x2(a0, a1);
+  hi = pack_bf16x2(a2, a3);
+}
+// Four E4M3 codes times the scale -> two bf16 pairs: each code pair through the exact E4M3 -> f16x2
+// conversion, widened to fp32, multiplied (one rounding), rounded to bf16.
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint64_t s2, uint32_t& lo, uint32_t& hi) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+  const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  float a0, a1, a2, a3;
+  f2_split(f2_mul(f2(f01.x, f01.y), s2), a0, a1);
+  f2_split(f2_mul(f2(f23.x, f23.y), s2), a2, a3);
+  lo = pack_bf16x2(a0, a1);
+  hi = pack_bf16x2(a2, a3);
+}
+// Dequantise key / value row `row` of a head_dim-128 tile in place: its 128 codes sit in column
+// block 1 (one 128-byte swizzled row), the bf16 row takes both 64-column blocks. The whole code row
+// is read before any of it is overwritten, and no other row is touched.
+template <int kQ>
+__device__ __forceinline__ void dequantize_row(uint8_t* tile, int row, float scale, bool valid) {
+  const uint32_t sw = (uint32_t)(row & 7);
+  uint4 cw[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) cw[u] = *reinterpret_cast<const uint4*>(tile + kRegion + row * 128 + ((u ^ sw) << 4));
+  const uint64_t s2 = f2(scale, scale);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {  // codes 16u .. 16u+15 -> bf16 units 2(u%4), 2(u%4)+1 of block u/4
+    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+    if (valid) {
+      if constexpr (kQ == 1) {
+        int8x4_to_bf16(cw[u].x, s2, o0.x, o0.y);
+        int8x4_to_bf16(cw[u].y, s2, o0.z, o0.w);
+        int8x4_to_bf16(cw[u].z, s2, o1.x, o1.y);
+        int8x4_to_bf16(cw[u].w, s2, o1.z, o1.w);
+      } else {
+        e4m3x4_to_bf16(cw[u].x, s2, o0.x, o0.y);
+        e4m3x4_to_bf16(cw[u].y, s2, o0.z, o0.w);
+        e4m3x4_to_bf16(cw[u].z, s2, o1.x, o1.y);
+        e4m3x4_to_bf16(cw[u].w, s2, o1.z, o1.w);
+      }
+    }
+    uint8_t* blk = tile + (u >> 2) * kRegion + row * 128;
+    const uint32_t k0 = 2u * (uint32_t)(u & 3);
+    *reinterpret_cast<uint4*>(blk + ((k0 ^ sw) << 4)) = o0;
+    *reinterpret_cast<uint4*>(blk + (((k0 + 1) ^ sw) << 4)) = o1;
+  }
+}
+
 // kPrefix: the cascade's shared-prefix pass (one request of num_tokens query rows that all
 // see the whole prefix; unnormalised partials out instead of normalised rows).
-template <bool kPrefix, int kD>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kPrefix, int kD, int kQ = 0>
+__global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     varlen_tc_kernel(const __grid_constant__ VarlenParams p, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
-  constexpr int kTileBytes = Layout<kD>::kTileBytes;
-  constexpr int kOffQ = Layout<kD>::kOffQ;
-  constexpr int kOffK = Layout<kD>::kOffK;
-  constexpr int kOffV = Layout<kD>::kOffV;
-  constexpr int kOffBar = Layout<kD>::kOffBar;
+  static_assert(kQ == 0 || (kD == 128 && !kPrefix), "8-bit caches: head_dim 128, no prefix mode");
+  constexpr int kTileBytes = Layout<kD, kQ>::kTileBytes;
+  constexpr int kOffQ = Layout<kD, kQ>::kOffQ;
+  constexpr int kOffK = Layout<kD, kQ>::kOffK;
+  constexpr int kOffV = Layout<kD, kQ>::kOffV;
+  constexpr int kOffScale = Layout<kD, kQ>::kOffScale;
+  constexpr int kOffBar = Layout<kD, kQ>::kOffBar;
   constexpr int kBlocks = kD / 64;  // 64-column blocks of a row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -196,10 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars[B_Q], 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[B_KF + s], 1);
-      mbar_init(&bars[B_VF + s], 1);
+      // 8-bit caches: the producer's 32 lanes' scale copies arrive on the full barriers too
+      mbar_init(&bars[B_KF + s], kQ != 0 ? 33 : 1);
+      mbar_init(&bars[B_VF + s], kQ != 0 ? 33 : 1);
       mbar_init(&bars[B_KE + s], 1);
       mbar_init(&bars[B_VE + s], 1);
+      mbar_init(&bars[B_KR + s], 64);
+      mbar_init(&bars[B_VR + s], 64);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[B_SF + t], 1);
@@ -243,13 +331,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg = (j0 + i) * pages_per_tile + lane;
       return (lane < pages_per_tile && pg < seq_pages) ? __ldg(table + pg) : 0;
     };
+    // 8-bit caches: a tile's 128 key (or value) scales, 4 per lane, copied asynchronously into
+    // shared memory with completion on the tile's full barrier; positions past the sequence end,
+    // or on a page outside the pool, are zero-filled instead of read
+    auto copy_scales = [&](int i, int st, int page, const float* base, float* dst, uint64_t* bar) {
+      const int key = 4 * lane;
+      const int pg = __shfl_sync(0xffffffffu, page, key / bs);  // the lane holding this key's page
+      const int pos0 = (j0 + i) * kBN + key;
+      const bool pg_ok = pg >= 0 && pg < p.num_blocks;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool take = pg_ok && pos0 + e < seq_len;
+        const float* src = take ? base + ((size_t)pg * bs + (key + e) % bs) * p.num_kv_heads + kvh : base;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst + st * 256 + key + e)),
+                     "l"(src), "r"(take ? 4 : 0)
+                     : "memory");
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+    };
+    float* scales = reinterpret_cast<float*>(smem + kOffScale);  // [stage][K 128 | V 128]
     int cur = n_kv > 0 ? page_of(0) : 0;
     for (int i = 0; i < n_kv; ++i) {
       const int st = i % kStages;
       const uint32_t round_parity = ((i / kStages) - 1) & 1;
       const int p0 = (j0 + i) * pages_per_tile;
       const int np = min(p0 + pages_per_tile, seq_pages) - p0;
-      const uint32_t bytes = (uint32_t)np * bs * (uint32_t)(kD * 2);
+      const uint32_t bytes = (uint32_t)np * bs * (uint32_t)(kQ != 0 ? kD : kD * 2);
       const int nxt = i + 1 < n_kv ? page_of(i + 1) : 0;
       if (i >= kStages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
         if (lane == 0) set_abort(abort_flag, p.err);
@@ -259,10 +366,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < np) {
         if (cur < 0 || cur >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
-        for (int a = 0; a < kBlocks; ++a)
-          tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st],
-                      a * 64, kvh, 0, cur);
+        if constexpr (kQ != 0) {  // the page's codes: one 128-byte row per key, into column block 1
+          tma_load_4d(smem + kOffK + st * kTileBytes + kRegion + lane * bs * 128, &kmap, &bars[B_KF + st], 0, kvh,
+                      0, cur);
+        } else {
+          for (int a = 0; a < kBlocks; ++a)
+            tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st],
+                        a * 64, kvh, 0, cur);
+        }
       }
+      if constexpr (kQ != 0) copy_scales(i, st, cur, p.k_scales, scales, &bars[B_KF + st]);
       if (i >= kStages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
         if (lane == 0) {
           set_abort(abort_flag, p.err);
@@ -272,10 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
       __syncwarp();
-      if (lane < np)
-        for (int a = 0; a < kBlocks; ++a)
-          tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st],
-                      a * 64, kvh, 0, cur);
+      if (lane < np) {
+        if constexpr (kQ != 0) {
+          tma_load_4d(smem + kOffV + st * kTileBytes + kRegion + lane * bs * 128, &vmap, &bars[B_VF + st], 0, kvh,
+                      0, cur);
+        } else {
+          for (int a = 0; a < kBlocks; ++a)
+            tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st],
+                        a * 64, kvh, 0, cur);
+        }
+      }
+      if constexpr (kQ != 0) copy_scales(i, st, cur, p.v_scales, scales + 128, &bars[B_VF + st]);
       __syncwarp();
       if (lane == 0) *issued_tiles = i + 1;
       cur = nxt;
@@ -321,7 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto commit_if = [&](bool cond, int bar) {
       if (cond && lane == 0) umma_commit(&bars[bar]);
     };
-    bool ok = warp_wait(&bars[B_Q], 0, abort_flag) && warp_wait(&bars[B_KF], 0, abort_flag);
+    // 8-bit caches: a tile is ready for the tensor core once the converters have dequantised it
+    constexpr int kReadyK = kQ != 0 ? B_KR : B_KF;
+    constexpr int kReadyV = kQ != 0 ? B_VR : B_VF;
+    bool ok = warp_wait(&bars[B_Q], 0, abort_flag) && warp_wait(&bars[kReadyK], 0, abort_flag);
     if (ok) {
       tc_fence_after();
       if (nA > 0) issue_s(0, 0);
@@ -331,9 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; ok && j < n_kv; ++j) {
       const int st = j % kStages;
-      if (!(ok = warp_wait(&bars[B_VF + st], (j / kStages) & 1, abort_flag))) break;
+      if (!(ok = warp_wait(&bars[kReadyV + st], (j / kStages) & 1, abort_flag))) break;
       const int zero_from = seq_len - (j0 + j) * kBN;  // V rows at or past the sequence end: exact zeros
-      if (zero_from < kBN) {
+      if (kQ == 0 && zero_from < kBN) {  // (8-bit caches: the converters write those rows as zeros)
         uint8_t* vbp = smem + kOffV + st * kTileBytes;
         const int rows = kBN - zero_from;
         for (int i = lane; i < rows * (kD / 8); i += 32) {
@@ -350,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool next = j + 1 < n_kv;
       if (next) {
-        if (!(ok = warp_wait(&bars[B_KF + (j + 1) % kStages], ((j + 1) / kStages) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(&bars[kReadyK + (j + 1) % kStages], ((j + 1) / kStages) & 1, abort_flag))) break;
         tc_fence_after();
         if (j + 1 < nA) issue_s(0, j + 1);
       }
@@ -367,6 +490,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit_if(j + 1 + kStages < n_kv, B_KE + (j + 1) % kStages);
       }
       __syncwarp();
+    }
+    if (!ok) set_abort(abort_flag, p.err);
+  } else if (kQ != 0 && warp >= 10) {
+    // ------------------------------------------------ 8-bit caches: warps 10-11 dequantise each
+    // K and V tile in place ("32. Production attention kernels", Quantized KV caches: the tile of
+    // codes times its per-slot scale, then used exactly like a bf16 tile): thread c takes rows c
+    // and c + 64; rows at or past the sequence end become zeros (a stale slot may hold anything)
+    const int c = tid - 320;
+    const float* scales = reinterpret_cast<const float*>(smem + kOffScale);
+    bool ok = true;
+    for (int i = 0; ok && i < n_kv; ++i) {
+      const int st = i % kStages;
+      const int key0 = (j0 + i) * kBN;
+      for (int kv = 0; kv < 2; ++kv) {
+        if (!warp_wait(&bars[(kv ? B_VF : B_KF) + st], (i / kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* tile = smem + (kv ? kOffV : kOffK) + st * kTileBytes;
+        const float* sc = scales + st * 256 + kv * 128;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int row = c + 64 * h;
+          const bool valid = key0 + row < seq_len;
+          dequantize_row<kQ>(tile, row, valid ? sc[row] : 0.f, valid);
+        }
+        fence_async_smem();  // generic-proxy writes, read next by the tensor core
+        mbar_arrive(&bars[(kv ? B_VR : B_KR) + st]);
+      }
     }
     if (!ok) set_abort(abort_flag, p.err);
   } else {
@@ -684,25 +836,26 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const __grid_
   for (int i = total + tid; i < a.capacity; i += kPlanThreads) a.items[i] = -1;
 }
 
-template <bool kPrefix, int kD>
+template <bool kPrefix, int kD, int kQ = 0>
 cudaError_t launch_pair(const VarlenParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                         const CUtensorMap& vmap, long long ctas, cudaStream_t stream) {
   // the shared-memory opt-in is per device and kernel; setting it twice is harmless
   static std::atomic<bool> attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  constexpr int smem = Layout<kD>::kSmemBytes;
+  constexpr int smem = Layout<kD, kQ>::kSmemBytes;
+  constexpr int threads = kQ != 0 ? kThreadsQ : kThreads;
   if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(varlen_tc_kernel<kPrefix, kD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem);
+    cudaError_t e = cudaFuncSetAttribute(varlen_tc_kernel<kPrefix, kD, kQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
   if (!p.plan_on_device) {
-    varlen_tc_kernel<kPrefix, kD><<<(unsigned)ctas, kThreads, smem, stream>>>(p, qmap, kmap, vmap);
+    varlen_tc_kernel<kPrefix, kD, kQ><<<(unsigned)ctas, threads, smem, stream>>>(p, qmap, kmap, vmap);
     return cudaGetLastError();
   }
-  return launch_dependent(varlen_tc_kernel<kPrefix, kD>, (unsigned)ctas, kThreads, smem, stream, p, qmap, kmap,
+  return launch_dependent(varlen_tc_kernel<kPrefix, kD, kQ>, (unsigned)ctas, threads, smem, stream, p, qmap, kmap,
                           vmap);
 }
 }  // namespace
@@ -747,6 +900,11 @@ cudaError_t launch_varlen_tc(const VarlenParams& p_in, const CUtensorMap& qmap, 
                          p.num_kv_heads;
   if (ctas <= 0) return cudaSuccess;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (p.quant != 0) {  // 8-bit caches: head_dim 128, the two-tile kernel with its converter warps
+    if (p.head_dim != 128 || p.prefix_mode) return cudaErrorInvalidValue;
+    return p.quant == 1 ? launch_pair<false, 128, 1>(p, qmap, kmap, vmap, ctas, stream)
+                        : launch_pair<false, 128, 2>(p, qmap, kmap, vmap, ctas, stream);
+  }
   if (p.head_dim == 256) {
     if (p.prefix_mode) return cudaErrorInvalidValue;
     return launch_varlen_tc256(p, qmap, kmap, vmap, ctas, stream);

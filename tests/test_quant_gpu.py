@@ -137,3 +137,69 @@ def test_decode_long_diffuse_attention_with_one_sign_queries(kind, keys):
         # the bf16 budget (the offset's rounding, ~1152 x the values' scale x 2^-24 per add)
         err = (out[0].double().cpu() - want[0]).abs().max().item()
         assert err <= 2e-3, f"{kind} alike keys, 8192-key row: max abs {err:.3e}"
+
+
+Q_LENS = [37, 1, 5, 0, 130, 300, 64, 1, 129]
+SEQ_LENS = [90, 700, 2000, 3, 900, 300, 1000, 17, 129]
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_tensor_core_shapes(kind, G, bs, causal):
+    """8-bit caches on the tensor-core varlen kernel (head_dim 128): each K / V tile's codes are
+    dequantised in shared memory and used like a bf16 tile; every row against the oracle over the
+    dequantised cache, for every group and block size, causal and not."""
+    hkv = 2 if G <= 8 else 1
+    case = workloads.make_case("qvt", 760 + 10 * G + bs, Q_LENS, SEQ_LENS, num_q_heads=G * hkv, num_kv_heads=hkv,
+                               head_dim=128, block_size=bs, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    out = pa.paged_attention_varlen_quant(case.q.to(DEV), kc, vc, ks, vs, case.query_start_loc.to(DEV),
+                                          case.seq_lens.to(DEV), case.block_tables.to(DEV), case.max_query_len,
+                                          causal, case.scale)
+    want = quant.paged_attention_varlen_quant(case.q, ko, vo, kso, vso, case.query_start_loc, case.seq_lens,
+                                              case.block_tables, causal, case.scale)
+    check_close(out, want, torch.bfloat16, label=f"{kind} varlen G{G} bs{bs} causal={causal}")
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("window,softcap,sinks", [(100, 0.0, False), (0, 30.0, False), (0, 0.0, True),
+                                                  (37, 20.0, True)])
+def test_varlen_tensor_core_modifiers(kind, window, softcap, sinks):
+    case = workloads.make_case("qvm", 800 + window, Q_LENS, SEQ_LENS, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    sk = torch.linspace(-2.0, 3.0, 32, dtype=torch.float32) if sinks else None
+    out = pa.paged_attention_varlen_quant(case.q.to(DEV), kc, vc, ks, vs, case.query_start_loc.to(DEV),
+                                          case.seq_lens.to(DEV), case.block_tables.to(DEV), case.max_query_len,
+                                          True, case.scale, window=window, softcap=softcap,
+                                          sinks=None if sk is None else sk.to(DEV))
+    want = quant.paged_attention_varlen_quant(case.q, ko, vo, kso, vso, case.query_start_loc, case.seq_lens,
+                                              case.block_tables, True, case.scale, window=window, softcap=softcap,
+                                              sinks=sk)
+    check_close(out, want, torch.bfloat16, label=f"{kind} varlen w{window} cap{softcap} sinks{sinks}")
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_varlen_long_prompt_and_head_dim_256(kind):
+    """A 3,000-token causal prompt plus a 1,000-token chunk on the tensor-core path (every row), and
+    the head_dim-256 shape, which runs as per-token decodes over the codes."""
+    case = workloads.make_case("qvl", 830, [3000, 1000], [3000, 3000], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                               block_size=64, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    out = pa.paged_attention_varlen_quant(case.q.to(DEV), kc, vc, ks, vs, case.query_start_loc.to(DEV),
+                                          case.seq_lens.to(DEV), case.block_tables.to(DEV), case.max_query_len,
+                                          True, case.scale)
+    want = quant.paged_attention_varlen_quant(case.q, ko, vo, kso, vso, case.query_start_loc, case.seq_lens,
+                                              case.block_tables, True, case.scale)
+    check_close(out, want, torch.bfloat16, label=f"{kind} varlen long")
+    c2 = workloads.make_case("qv256", 831, [37, 1, 130], [90, 700, 400], num_q_heads=16, num_kv_heads=4,
+                             head_dim=256, block_size=16, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(c2, kind)
+    out = pa.paged_attention_varlen_quant(c2.q.to(DEV), kc, vc, ks, vs, c2.query_start_loc.to(DEV),
+                                          c2.seq_lens.to(DEV), c2.block_tables.to(DEV), c2.max_query_len, True,
+                                          c2.scale)
+    want = quant.paged_attention_varlen_quant(c2.q, ko, vo, kso, vso, c2.query_start_loc, c2.seq_lens,
+                                              c2.block_tables, True, c2.scale)
+    check_close(out, want, torch.bfloat16, label=f"{kind} varlen D256")
