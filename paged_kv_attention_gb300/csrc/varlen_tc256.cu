@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           if (!is_v) {
-            // S(j) = Q K(j)^T into block blk: K steps 0-7 from the low half of K, 8-15 from the high
+            // S(j) = Q K(j)^T into block blk: K steps 0-7 from the low half of K, 8-15 from the high.
+            // Each half's slot is released as soon as the MMAs that read it are done, so the
+            // producer can refill the low half's slot while the high half is still being read.
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               const int half = kk >> 3;
@@ -315,27 +317,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t offq = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
               const uint64_t offk = (uint64_t)((((kk >> 2) & 1) * kRegion + (kk & 3) * 32) >> 4);
               umma_ss(tmem + col_s(blk), dq0 + offq, dk + offk, id_s, kk > 0 ? 1u : 0u);
+              if (kk == 7) release(it);
             }
             umma_commit(&bars[B_SF + blk]);
+            release(it + 1);
             // the first tile's last S: the query buffer may be refilled with the second tile's
             if (t == 0 && n_tiles == 2 && j == u.n - 1) umma_commit(&bars[B_QE]);
           } else {
-            // O += P(j) V(j): 8 key steps, each two N=128 MMAs (one per half of V)
+            // O += P(j) V(j): all 8 key steps of the low half of V (output columns 0-127), then of
+            // the high half, each half's slot released once its MMAs are done
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
+              for (int kk = 0; kk < kBN / 16; ++kk) {
                 const uint64_t dv = dring_v + (uint64_t)((((it + h) % kSlots) * kHalfBytes + kk * 2048) >> 4);
                 umma_ts(tmem + kColO + h * 128, tmem + col_s(blk) + 8 * kk, dv, id_pv,
                         (j > 0 || kk > 0) ? 1u : 0u);
               }
+              if (h == 0) release(it);
             }
             umma_commit(&bars[B_OD]);
             if (j == u.n - 1) umma_commit(&bars[B_OF]);
+            release(it + 1);
           }
         }
-        release(it);
-        release(it + 1);
         __syncwarp();
       }
     }
