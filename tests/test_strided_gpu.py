@@ -81,22 +81,30 @@ def varlen_case(seed, q_lens, seq_lens, hq, hkv, d, bs, dtype):
 
 VARLEN_SHAPES = [(128, 32, 8, 16, torch.bfloat16),   # tensor-core kernel
                  (128, 16, 2, 64, torch.bfloat16),   # tensor-core kernel, group 8
-                 (64, 8, 2, 16, torch.bfloat16),     # one-split decode per token
+                 (64, 8, 2, 16, torch.bfloat16),     # tensor-core kernel at head_dim 64
+                 (256, 16, 4, 32, torch.bfloat16),   # the head_dim-256 tensor-core kernel
                  (128, 8, 8, 16, torch.float32)]     # fp32: one-split decode per token
 
 
 @pytest.mark.parametrize("d,hq,hkv,bs,dtype", VARLEN_SHAPES)
-@pytest.mark.parametrize("split_decodes", [False, True])
+@pytest.mark.parametrize("split_decodes", [False, True, "tensor"])
 def test_varlen_strided_equals_dense(d, hq, hkv, bs, dtype, split_decodes):
+    """(split_decodes "tensor": the device-planned grid with every request on the tensor cores.)"""
+    if split_decodes == "tensor":
+        if dtype != torch.bfloat16:
+            pytest.skip("schedules are a bf16 tensor-core feature")
+        kw = dict(schedule="tensor")
+    else:
+        kw = dict(split_decodes=split_decodes)
     q_lens = [1, 5, 37, 130, 1, 0, 64]
     seq_lens = [700, 5, 37, 900, 1, 3, 200]
     case = varlen_case(950 + d + hq + bs, q_lens, seq_lens, hq, hkv, d, bs, dtype)
     kc, vc = gpu_pools(case)
     args = (kc, vc, case.query_start_loc.to(DEV), case.seq_lens.to(DEV), case.block_tables.to(DEV), max(q_lens))
-    dense = pa.paged_attention_varlen(case.q.to(DEV), *args, True, case.scale, split_decodes=split_decodes)
+    dense = pa.paged_attention_varlen(case.q.to(DEV), *args, True, case.scale, **kw)
     _, qv = fused_qkv(case)
     obuf, ov = wide_out(qv)
-    pa.paged_attention_varlen(qv, *args, True, case.scale, out=ov, split_decodes=split_decodes)
+    pa.paged_attention_varlen(qv, *args, True, case.scale, out=ov, **kw)
     assert torch.equal(ov, dense)
     assert untouched(obuf, hq)
 
