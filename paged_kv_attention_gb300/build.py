@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedattn.so")
-SOURCES = ["pa_api.cu", "cache_write.cu", "decode.cu", "varlen_tc.cu", "varlen_tc256.cu", "decode_static_scratch.cu"]
+SOURCES = ["pa_api.cu", "cache_write.cu", "decode.cu", "decode_seg.cu", "varlen_tc.cu", "varlen_tc256.cu",
+           "decode_static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -904,6 +904,27 @@ extern "C" pa_status pa_paged_attention_decode_quant(const void* q, const void* 
   p.scale_log2 = sc * kLog2e;
   st = apply_options(options, sc, p);
   if (st != PA_OK) return st;
+  if (num_splits == 0 && decode_seg_supported(head_dim, p.group, num_seqs, p.quant)) {
+    // automatic splitting: balanced segments, every CTA that fits at once taking the same share of
+    // the batch's chunks (with one split per sequence the 8-bit decode's last wave runs part full)
+    DeviceInfo* info = nullptr;
+    if (!device_info(&info)) return PA_ERR_CUDA;
+    const int X = std::max(1, info->sms * decode_seg_ctas_per_sm(p.quant) / num_kv_heads);
+    const size_t need = decode_seg_workspace_bytes(num_seqs, num_q_heads, X);
+    if (workspace != nullptr && workspace_bytes >= need && aligned16(workspace)) {
+      p.seg_ctas = X;
+      p.ws_acc = static_cast<float*>(workspace);
+      p.ws_ml = p.ws_acc + (size_t)X * 2 * num_q_heads * head_dim;
+      p.seg_off = reinterpret_cast<int32_t*>(p.ws_ml + (size_t)X * 2 * num_q_heads * 2);
+      p.q_stride = (long long)num_q_heads * head_dim;
+      p.out_stride = (long long)num_q_heads * head_dim;
+      CUtensorMap kmap, vmap;
+      if (!encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk, 1) ||
+          !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk, 1))
+        return PA_ERR_CUDA;
+      return launch_decode_seg(p, kmap, vmap, as_stream(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+  }
   return run_decode_units(p, PA_DTYPE_BF16, k_cache, v_cache, num_splits, workspace, workspace_bytes,
                           as_stream(stream));
 }

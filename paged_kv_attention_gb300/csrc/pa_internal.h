@@ -71,6 +71,10 @@ struct DecodeParams {
   // not read from; its CTAs wait for that kernel's completion only before they exit, so that
   // this grid's completion implies the previous one's (the combine after it reads both)
   int overlap_previous;
+  // balanced segments (8-bit caches, decode): CTAs per KV head, and the chunk offsets of the
+  // sequences the decode grid leaves in the workspace for its combine
+  int seg_ctas;
+  int32_t* seg_off;
 };
 
 // key_stride / value_stride: bytes from one token's row to the next (multiples of 16)
@@ -94,6 +98,15 @@ int decode_bf16_ctas_per_sm(int head_dim, int group, int quant);
 // fp32 CUDA-core decode.
 cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream);
 int decode_f32_ctas_per_sm(int head_dim, int group);
+
+// Balanced-segment decode over 8-bit caches (decode_seg.cu): every resident CTA of a KV head streams
+// an equal share of the batch's chunks, followed by its combine. p.seg_ctas, ws_acc / ws_ml and
+// seg_off must be set (see decode_seg_workspace_bytes).
+bool decode_seg_supported(int head_dim, int group, int num_units, int quant);
+int decode_seg_ctas_per_sm(int quant);
+size_t decode_seg_workspace_bytes(int num_units, int num_q_heads, int ctas_per_head);
+cudaError_t launch_decode_seg(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream);
 
 // log-sum-exp merge of split partials into out.
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);

@@ -203,3 +203,77 @@ def test_varlen_long_prompt_and_head_dim_256(kind):
     want = quant.paged_attention_varlen_quant(c2.q, ko, vo, kso, vso, c2.query_start_loc, c2.seq_lens,
                                               c2.block_tables, True, c2.scale)
     check_close(out, want, torch.bfloat16, label=f"{kind} varlen D256")
+
+
+# Automatic splitting of an 8-bit decode at head_dim 128 (groups <= 8) runs as balanced segments:
+# every resident CTA of a KV head streams the same share of the batch's chunks, sequences cut between
+# CTAs are merged by the combine. These cases put sequence boundaries everywhere relative to the CTA
+# ranges: empty contexts, one-chunk contexts, one long sequence spread over every CTA, thousands of
+# short ones.
+SEG_LENS = {
+    "ragged": [1, 15, 16, 17, 300, 2049, 0, 4096, 33, 0, 1000, 7],
+    "one_long": [8191],
+    "many_short": [int(x) for x in torch.randint(0, 70, (3000,), generator=torch.Generator().manual_seed(5))],
+    "uniform": [4096] * 24,
+}
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("lens", list(SEG_LENS))
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2)])
+def test_decode_balanced_segments(kind, lens, hq, hkv):
+    L = SEG_LENS[lens]
+    case = workloads.decode_case("qseg", 900 + len(L) + hq, L, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                                 block_size=16, dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                          case.seq_lens.to(DEV), case.scale, num_splits=0, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    seqs = list(range(case.num_reqs)) if case.num_reqs <= 64 else list(range(0, case.num_reqs, 7))
+    want = quant.paged_attention_decode_quant(case.q, ko, vo, kso, vso, case.block_tables, case.seq_lens, case.scale,
+                                              seqs=seqs)
+    rows = torch.tensor(seqs)
+    check_close(out, want, torch.bfloat16, rows=rows, label=f"{kind} segments {lens} G{hq // hkv}")
+    empty = [s for s in seqs if L[s] == 0]
+    if empty:
+        assert torch.equal(out[empty].float(), torch.zeros_like(out[empty].float()))
+    # the explicit one-split grid computes the same rows within the tolerance
+    ref = pa.paged_attention_decode_quant(case.q.to(DEV), kc, vc, ks, vs, case.block_tables.to(DEV),
+                                          case.seq_lens.to(DEV), case.scale, num_splits=1)
+    assert (out.float() - ref.float()).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_decode_balanced_segments_with_modifiers_and_graph_replay(kind):
+    """Window, softcap and sinks on the segment path; a captured call replays correctly after the
+    context lengths change (the segments are recomputed from the device lengths at every run)."""
+    full = [3000, 40, 1500, 0, 2222, 17]
+    case = workloads.decode_case("qsegm", 930, full, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=32,
+                                 dtype=torch.bfloat16)
+    (kc, vc, ks, vs), (ko, vo, kso, vso) = filled(case, kind)
+    sinks = torch.randn(32, generator=torch.Generator().manual_seed(2))
+    sinks_dev = sinks.to(DEV)  # (a host-to-device copy inside the capture would invalidate it)
+    q, tables = case.q.to(DEV), case.block_tables.to(DEV)
+    lens = torch.tensor([1000, 40, 1500, 0, 2000, 1], dtype=torch.int32, device=DEV)
+    out = torch.empty_like(q)
+    ws = torch.empty(pa.decode_workspace_bytes(6, 32, 128, tables.shape[1], 32, 0), dtype=torch.uint8, device=DEV)
+
+    def call():
+        pa.paged_attention_decode_quant(q, kc, vc, ks, vs, tables, lens, case.scale, out=out, workspace=ws,
+                                        window=700, softcap=30.0, sinks=sinks_dev)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for new in ([1000, 40, 1500, 0, 2000, 1], [3000, 1, 900, 5, 2222, 17], [0, 0, 0, 0, 0, 8]):
+        lens.copy_(torch.tensor(new, dtype=torch.int32))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        want = quant.paged_attention_decode_quant(case.q, ko, vo, kso, vso, case.block_tables,
+                                                  torch.tensor(new, dtype=torch.int32), case.scale, window=700,
+                                                  softcap=30.0, sinks=sinks.double())
+        check_close(out, want, torch.bfloat16, label=f"{kind} segments replay {new}")
