@@ -108,7 +108,7 @@ def source_hash(source: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_gb300", "csrc")
-    for name in (source, "pa_common.cuh", "tc_common.cuh"):
+    for name in (source, "pa_common.cuh", "tc_common.cuh", "decode_common.cuh"):
         try:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
@@ -903,7 +903,8 @@ def main():
             "workload": "decode_64x4096_int8 (same queries and tokens, int8 codes + fp32 scales)",
             "value": round(q8["gbs"], 2), "unit": "GB/s", "call_ms": round(q8["ms"], 5),
             "algorithmic_bytes_per_launch": q8["bytes"], "frac_of_hbm_peak": round(q8["gbs"] / hbm, 4),
-            "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3), "traffic": traffic.get("decode_int8_kernel")}
+            "speedup_vs_bf16_call": round(d["call_ms"] / q8["ms"], 3), "traffic": traffic.get("decode_seg_kernel"),
+            "kernel": "decode_seg_kernel<int8> + combine_seg_kernel (balanced segments)"}
     if f8 is not None:
         line["decode_fp8"] = {
             "workload": "decode_64x4096_fp8_e4m3 (same queries and tokens, E4M3 codes + fp32 scales)",
