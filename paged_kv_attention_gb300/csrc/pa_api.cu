@@ -53,6 +53,33 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs
   return r == CUDA_SUCCESS;
 }
 
+// The same bf16 pool viewed as a 5-D tensor (64 columns, 8 rows, D / 64 column blocks, row
+// groups of 8 across the pool, Hkv) so that one box is a whole page of one KV head (bs <= 128
+// rows, every column block) landing as [row group][column block][8 rows x 128 bytes]: one copy
+// per page instead of one per 64-column block. Each 8-row x 128-byte block is a 128-byte-swizzle
+// atom; row groups sit 256 * D / 64 bytes apart, column blocks 1,024 bytes apart.
+bool encode_cache_map_pages(CUtensorMap* map, const void* base, int D, int Hkv, int bs, int num_blocks) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || bs % 8 != 0 || bs > 128 || D % 64 != 0) return false;
+  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+  cuuint64_t dims[5] = {64, 8, (cuuint64_t)D / 64, (cuuint64_t)num_blocks * bs / 8, (cuuint64_t)Hkv};
+  cuuint64_t strides[4] = {row, 128, 8 * row, (cuuint64_t)D * 2};
+  cuuint32_t box[5] = {64, 8, (cuuint32_t)D / 64, (cuuint32_t)bs / 8, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The bf16 K / V maps of the tensor-core varlen kernels: whole-page boxes at head_dim 128, one
+// box per page and 64-column block otherwise (head_dim 64 has one block; the head_dim-256 kernel
+// keeps its own layout).
+bool encode_varlen_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs, int num_blocks) {
+  if (D == 128) return encode_cache_map_pages(map, base, D, Hkv, bs < 128 ? bs : 128, num_blocks);
+  return encode_cache_map(map, base, D, Hkv, bs, num_blocks, bs < 128 ? bs : 128);
+}
+
 // q [N, Hq, D] bf16 (rows row_stride elements apart) viewed as (D, Hq, N); one box = `tokens`
 // tokens x `group` heads x 64 cols.
 bool encode_query_map(CUtensorMap* map, const void* base, int D, int Hq, int N, int group, int tokens,
@@ -714,10 +741,8 @@ pa_status varlen_impl(const void* q, const void* k_cache, const void* v_cache, c
     if (st != PA_OK) return st;
     CUtensorMap qmap, kmap, vmap;
     if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_tokens, G, tokens_per_tile, q_stride) ||
-        !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks,
-                          block_size < 128 ? block_size : 128) ||
-        !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks,
-                          block_size < 128 ? block_size : 128))
+        !encode_varlen_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks) ||
+        !encode_varlen_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks))
       return PA_ERR_CUDA;
     DecodeParams dp{};
     if (split_decodes) {
@@ -1129,8 +1154,8 @@ extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const
   vp.slot_count = slots;
   CUtensorMap qmap, kmap, vmap;
   if (!encode_query_map(&qmap, q, head_dim, num_q_heads, num_seqs, G, 128 / G, (long long)num_q_heads * head_dim) ||
-      !encode_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, block_size) ||
-      !encode_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, block_size))
+      !encode_varlen_cache_map(&kmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks) ||
+      !encode_varlen_cache_map(&vmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks))
     return PA_ERR_CUDA;
   if (launch_varlen_tc(vp, qmap, kmap, vmap, strm) != cudaSuccess) return PA_ERR_CUDA;
 

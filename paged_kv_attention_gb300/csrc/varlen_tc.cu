@@ -43,23 +43,26 @@ using namespace tc;
 constexpr int kBM = 128;  // packed query rows per tile
 constexpr int kStages = 2;
 constexpr int kRegion = 128 * 128;  // one [128 rows][64 bf16] swizzled 64-column block: 16 KiB
+constexpr int kLoneStages = 3;  // a CTA whose second query tile is empty keeps three K/V stages
 enum {
   B_Q = 0,
-  B_KF = 1,   // +stage
-  B_VF = 3,   // +stage
-  B_KE = 5,   // +stage
-  B_VE = 7,   // +stage
-  B_SF = 9,   // +tile (A, B)
-  B_PR = 11,  // +tile
-  B_OD = 13,  // +tile
-  B_FIN = 15,
-  B_KR = 16,  // +stage: 8-bit caches, the K tile is dequantised to bf16 (64 converter arrivals)
-  B_VR = 18,  // +stage: the same for V
-  kNumBars = 20
+  B_KF = 1,   // +stage (3)
+  B_VF = 4,   // +stage
+  B_KE = 7,   // +stage
+  B_VE = 10,  // +stage
+  B_SF = 13,  // +tile (A, B); a lone tile: +score block
+  B_PR = 15,  // +tile; a lone tile: +score block
+  B_OD = 17,  // +tile
+  B_FIN = 19,
+  B_KR = 20,  // +stage: 8-bit caches, the K tile is dequantised to bf16 (64 converter arrivals)
+  B_VR = 22,  // +stage: the same for V
+  kNumBars = 24
 };
 // Shared-memory layout for head dim kD (64 or 128): a tile of 128 rows is kD / 64 column blocks.
 // kQ (8-bit caches: 1 int8, 2 fp8 E4M3): a stage's codes land in its second column block and
 // are dequantised in place; its 128 key and 128 value scales sit after the V ring.
+// bf16 tiles (kQ 0): a lone tile's third K stage takes Q_B's place and its third V stage the
+// region after the barriers.
 template <int kD, int kQ = 0>
 struct Layout {
   static constexpr int kTileBytes = (kD / 64) * kRegion;
@@ -68,7 +71,19 @@ struct Layout {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffScale = kOffV + kStages * kTileBytes;
   static constexpr int kOffBar = kOffScale + (kQ != 0 ? kStages * 256 * 4 : 0);
-  static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 32;
+  static constexpr int kOffV2 = (kOffBar + kNumBars * 8 + 32 + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = 1024 + (kQ == 0 ? kOffV2 + kTileBytes : kOffBar + kNumBars * 8 + 32);
+  static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
+  // stage st of K / V (st < kStages: the rings; st == kStages: a lone tile's third stage)
+  __device__ static constexpr int k_stage(int st) { return st < kStages ? kOffK + st * kTileBytes : kOffQ + kTileBytes; }
+  __device__ static constexpr int v_stage(int st) { return st < kStages ? kOffV + st * kTileBytes : kOffV2; }
+  // Inside a K / V tile: bf16 tiles at head dim 128 arrive one page per copy as [8-row group]
+  // [column block][8 rows x 128 bytes] (kWide), the others as [column block][128 rows x 128
+  // bytes]. kCB: from one 64-column block to the next; kSBO: from one 8-row group to the next.
+  static constexpr bool kWide = kQ == 0 && kD == 128;
+  static constexpr int kCB = kWide ? 1024 : kRegion;
+  static constexpr int kSBO = kWide ? 1024 * (kD / 64) : 1024;
+  __device__ static constexpr int at(int row, int cb) { return (row >> 3) * kSBO + cb * kCB + (row & 7) * 128; }
 };
 constexpr int kThreads = 320;
 constexpr int kThreadsQ = 384;  // 8-bit caches: two more warps dequantise the K / V tiles
@@ -257,6 +272,13 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
   const int nA = max(0, endA - j0);
   const int nB = spanB.n_kv > 0 ? max(0, endB - j0) : 0;
   const int n_kv = max(nA, nB);
+  // A lone tile (the pair's second tile is empty: decodes, verify blocks, a prompt's last tokens):
+  // tile B's score block doubles tile A's, so S(j + 1) runs on the tensor core during the softmax of
+  // tile j, and Q_B's buffer with the spare shared memory holds a third K/V stage.
+  constexpr bool kLoneOk = !kPrefix && kQ == 0;
+  const bool lone = kLoneOk && nB == 0;
+  const int n_stages = lone ? kLoneStages : kStages;
+  using L = Layout<kD, kQ>;
   const int bs = p.block_size;
   const int pages_per_tile = kBN / bs;
   const int seq_pages = (seq_len + bs - 1) / bs;
@@ -280,12 +302,14 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     mbar_init(&bars[B_Q], 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kLoneStages; ++s) {
       // 8-bit caches: the producer's 32 lanes' scale copies arrive on the full barriers too
       mbar_init(&bars[B_KF + s], kQ != 0 ? 33 : 1);
       mbar_init(&bars[B_VF + s], kQ != 0 ? 33 : 1);
       mbar_init(&bars[B_KE + s], 1);
       mbar_init(&bars[B_VE + s], 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[B_KR + s], 64);
       mbar_init(&bars[B_VR + s], 64);
     }
@@ -319,8 +343,8 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      mbar_arrive_expect_tx(&bars[B_Q], 2 * kTileBytes);
-      for (int t = 0; t < 2; ++t)
+      mbar_arrive_expect_tx(&bars[B_Q], (lone ? 1 : 2) * kTileBytes);
+      for (int t = 0; t < (lone ? 1 : 2); ++t)
         for (int a = 0; a < kBlocks; ++a)
           tma_load_3d(smem + kOffQ + t * kTileBytes + a * kRegion, &qmap, &bars[B_Q], a * 64, kvh * G,
                       q_start + tok0 + t * TOK);
@@ -352,13 +376,13 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     float* scales = reinterpret_cast<float*>(smem + kOffScale);  // [stage][K 128 | V 128]
     int cur = n_kv > 0 ? page_of(0) : 0;
     for (int i = 0; i < n_kv; ++i) {
-      const int st = i % kStages;
-      const uint32_t round_parity = ((i / kStages) - 1) & 1;
+      const int st = i % n_stages;
+      const uint32_t round_parity = ((i / n_stages) - 1) & 1;
       const int p0 = (j0 + i) * pages_per_tile;
       const int np = min(p0 + pages_per_tile, seq_pages) - p0;
       const uint32_t bytes = (uint32_t)np * bs * (uint32_t)(kQ != 0 ? kD : kD * 2);
       const int nxt = i + 1 < n_kv ? page_of(i + 1) : 0;
-      if (i >= kStages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
+      if (i >= n_stages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
         if (lane == 0) set_abort(abort_flag, p.err);
         break;
       }
@@ -367,16 +391,21 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       if (lane < np) {
         if (cur < 0 || cur >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
         if constexpr (kQ != 0) {  // the page's codes: one 128-byte row per key, into column block 1
-          tma_load_4d(smem + kOffK + st * kTileBytes + kRegion + lane * bs * 128, &kmap, &bars[B_KF + st], 0, kvh,
-                      0, cur);
+          tma_load_4d(smem + L::k_stage(st) + kRegion + lane * bs * 128, &kmap, &bars[B_KF + st], 0, kvh, 0,
+                      cur);
         } else {
-          for (int a = 0; a < kBlocks; ++a)
-            tma_load_4d(smem + kOffK + st * kTileBytes + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st],
-                        a * 64, kvh, 0, cur);
+          if constexpr (L::kWide) {  // the whole page (bs / 8 row groups) in one copy
+            tma_load_5d(smem + L::k_stage(st) + L::at(lane * bs, 0), &kmap, &bars[B_KF + st], 0, 0, 0, cur * (bs / 8),
+                        kvh);
+          } else {
+            for (int a = 0; a < kBlocks; ++a)
+              tma_load_4d(smem + L::k_stage(st) + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st], a * 64,
+                          kvh, 0, cur);
+          }
         }
       }
       if constexpr (kQ != 0) copy_scales(i, st, cur, p.k_scales, scales, &bars[B_KF + st]);
-      if (i >= kStages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
+      if (i >= n_stages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
         if (lane == 0) {
           set_abort(abort_flag, p.err);
           *issued_tiles = i + 1;  // K of iteration i is in flight
@@ -387,12 +416,17 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       __syncwarp();
       if (lane < np) {
         if constexpr (kQ != 0) {
-          tma_load_4d(smem + kOffV + st * kTileBytes + kRegion + lane * bs * 128, &vmap, &bars[B_VF + st], 0, kvh,
-                      0, cur);
+          tma_load_4d(smem + L::v_stage(st) + kRegion + lane * bs * 128, &vmap, &bars[B_VF + st], 0, kvh, 0,
+                      cur);
         } else {
-          for (int a = 0; a < kBlocks; ++a)
-            tma_load_4d(smem + kOffV + st * kTileBytes + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st],
-                        a * 64, kvh, 0, cur);
+          if constexpr (L::kWide) {  // the whole page (bs / 8 row groups) in one copy
+            tma_load_5d(smem + L::v_stage(st) + L::at(lane * bs, 0), &vmap, &bars[B_VF + st], 0, 0, 0, cur * (bs / 8),
+                        kvh);
+          } else {
+            for (int a = 0; a < kBlocks; ++a)
+              tma_load_4d(smem + L::v_stage(st) + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st], a * 64,
+                          kvh, 0, cur);
+          }
         }
       }
       if constexpr (kQ != 0) copy_scales(i, st, cur, p.v_scales, scales + 128, &bars[B_VF + st]);
@@ -410,88 +444,152 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     // Descriptors advance by adding (byte offset >> 4) to the start-address field; every
     // operand lies below 256 KiB of the shared window, so the 14-bit field never carries.
     const uint64_t dq0 = sdesc(sQ, 16, 1024);
-    const uint64_t dk0 = sdesc(sK, 16, 1024);
-    const uint64_t dv0 = sdesc(sV, kRegion, 1024);  // MN-major V: 64-column halves kRegion apart
-    // S_t(j) = Q_t K_j^T into S block t
-    auto issue_s = [&](int t, int j) {
-      if (lane == 0) {
-        const uint64_t dq = dq0 + (uint64_t)((t * kTileBytes) >> 4);
-        const uint64_t dk = dk0 + (uint64_t)(((j % kStages) * kTileBytes) >> 4);
+    const uint64_t dk0 = sdesc(sK, 16, L::kSBO);
+    const uint64_t dv0 = sdesc(sV, L::kCB, L::kSBO);  // MN-major V: 64-column blocks L::kCB apart
+    if (lone) {
+      // a lone tile: the two softmax groups take the key tiles in turn (tile j: group j & 1, its
+      // score block and its O block), so two softmaxes run at once. Issue order S(0), S(1), then
+      // per tile P.V(j), S(j + 2).
+      auto dk_of = [&](int st) { return sdesc(smem_addr(smem + L::k_stage(st)), 16, L::kSBO); };
+      auto dv_of = [&](int st) { return sdesc(smem_addr(smem + L::v_stage(st)), L::kCB, L::kSBO); };
+      // S(j) into block j & 1, then release its K stage (only if the producer will refill it)
+      auto issue_s1 = [&](int j) {
+        if (lane == 0) {
+          const uint64_t dk = dk_of(j % kLoneStages);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
-          umma_ss(tmem + col_s(t), dq + off, dk + off, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t offq = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+            const uint64_t offk = (uint64_t)(((kk >> 2) * L::kCB + (kk & 3) * 32) >> 4);
+            umma_ss(tmem + col_s(j & 1), dq0 + offq, dk + offk, id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars[B_SF + (j & 1)]);
+          if (j + kLoneStages < nA) umma_commit(&bars[B_KE + j % kLoneStages]);
         }
-        umma_commit(&bars[B_SF + t]);
-      }
-    };
-    // O_t += P_t(j) V_j (N = kD: every 64-column block of V), P_t from the first 64 TMEM
-    // columns of S block t
-    auto issue_pv = [&](int t, int j) {
-      if (lane == 0) {
-        const uint64_t dv = dv0 + (uint64_t)(((j % kStages) * kTileBytes) >> 4);
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + col_o<kD>(t), tmem + col_s(t) + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), id_pv,
-                  kk > 0 ? 1u : acc0);
-        umma_commit(&bars[B_OD + t]);
-      }
-    };
-    auto commit_if = [&](bool cond, int bar) {
-      if (cond && lane == 0) umma_commit(&bars[bar]);
-    };
-    // 8-bit caches: a tile is ready for the tensor core once the converters have dequantised it
-    constexpr int kReadyK = kQ != 0 ? B_KR : B_KF;
-    constexpr int kReadyV = kQ != 0 ? B_VR : B_VF;
-    bool ok = warp_wait(&bars[B_Q], 0, abort_flag) && warp_wait(&bars[kReadyK], 0, abort_flag);
-    if (ok) {
-      tc_fence_after();
-      if (nA > 0) issue_s(0, 0);
-      if (nB > 0) issue_s(1, 0);
-      commit_if(kStages < n_kv, B_KE + 0);
-      __syncwarp();
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int st = j % kStages;
-      if (!(ok = warp_wait(&bars[kReadyV + st], (j / kStages) & 1, abort_flag))) break;
-      const int zero_from = seq_len - (j0 + j) * kBN;  // V rows at or past the sequence end: exact zeros
-      if (kQ == 0 && zero_from < kBN) {  // (8-bit caches: the converters write those rows as zeros)
-        uint8_t* vbp = smem + kOffV + st * kTileBytes;
-        const int rows = kBN - zero_from;
-        for (int i = lane; i < rows * (kD / 8); i += 32) {
-          const int row = zero_from + i / (kD / 8), c = i % (kD / 8);
-          *reinterpret_cast<uint4*>(vbp + (c >> 3) * kRegion + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_async_smem();
+      };
+      bool ok = warp_wait(&bars[B_Q], 0, abort_flag);
+      for (int j = 0; ok && j < min(2, nA); ++j) {
+        if (!(ok = warp_wait(&bars[B_KF + j], 0, abort_flag))) break;
+        tc_fence_after();
+        issue_s1(j);
         __syncwarp();
       }
-      if (j < nA) {
-        if (!(ok = warp_wait(&bars[B_PR + 0], j & 1, abort_flag))) break;
+      for (int j = 0; ok && j < nA; ++j) {
+        const int st = j % kLoneStages;
+        if (!(ok = warp_wait(&bars[B_VF + st], (j / kLoneStages) & 1, abort_flag))) break;
+        const int zero_from = seq_len - (j0 + j) * kBN;  // V rows at or past the sequence end: exact zeros
+        if (zero_from < kBN) {
+          uint8_t* vbp = smem + L::v_stage(st);
+          const int rows = kBN - zero_from;
+          for (int i = lane; i < rows * (kD / 8); i += 32) {
+            const int row = zero_from + i / (kD / 8), c = i % (kD / 8);
+            *reinterpret_cast<uint4*>(vbp + L::at(row, c >> 3) + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (!(ok = warp_wait(&bars[B_PR + (j & 1)], (j >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        issue_pv(0, j);
+        if (lane == 0) {
+          const uint64_t dv = dv_of(st);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(tmem + col_o<kD>(j & 1), tmem + col_s(j & 1) + 8 * kk, dv + (uint64_t)((kk * 2 * L::kSBO) >> 4),
+                    id_pv, (j > 1 || kk > 0) ? 1u : 0u);
+          umma_commit(&bars[B_OD + (j & 1)]);
+          if (j + kLoneStages < nA) umma_commit(&bars[B_VE + st]);
+        }
+        // S(j + 2) overwrites P(j) in block j & 1: it is issued after P.V(j), which reads it first
+        if (j + 2 < nA) {
+          if (!(ok = warp_wait(&bars[B_KF + (j + 2) % kLoneStages], ((j + 2) / kLoneStages) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_s1(j + 2);
+        }
+        __syncwarp();
       }
-      const bool next = j + 1 < n_kv;
-      if (next) {
-        if (!(ok = warp_wait(&bars[kReadyK + (j + 1) % kStages], ((j + 1) / kStages) & 1, abort_flag))) break;
+      if (!ok) set_abort(abort_flag, p.err);
+    } else {
+      // S_t(j) = Q_t K_j^T into S block t
+      auto issue_s = [&](int t, int j) {
+        if (lane == 0) {
+          const uint64_t dq = dq0 + (uint64_t)((t * kTileBytes) >> 4);
+          const uint64_t dk = dk0 + (uint64_t)(((j % kStages) * kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t offq = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+            const uint64_t offk = (uint64_t)(((kk >> 2) * L::kCB + (kk & 3) * 32) >> 4);
+            umma_ss(tmem + col_s(t), dq + offq, dk + offk, id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars[B_SF + t]);
+        }
+      };
+      // O_t += P_t(j) V_j (N = kD: every 64-column block of V), P_t from the first 64 TMEM
+      // columns of S block t
+      auto issue_pv = [&](int t, int j) {
+        if (lane == 0) {
+          const uint64_t dv = dv0 + (uint64_t)(((j % kStages) * kTileBytes) >> 4);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(tmem + col_o<kD>(t), tmem + col_s(t) + 8 * kk, dv + (uint64_t)((kk * 2 * L::kSBO) >> 4), id_pv,
+                    kk > 0 ? 1u : acc0);
+          umma_commit(&bars[B_OD + t]);
+        }
+      };
+      auto commit_if = [&](bool cond, int bar) {
+        if (cond && lane == 0) umma_commit(&bars[bar]);
+      };
+      // 8-bit caches: a tile is ready for the tensor core once the converters have dequantised it
+      constexpr int kReadyK = kQ != 0 ? B_KR : B_KF;
+      constexpr int kReadyV = kQ != 0 ? B_VR : B_VF;
+      bool ok = warp_wait(&bars[B_Q], 0, abort_flag) && warp_wait(&bars[kReadyK], 0, abort_flag);
+      if (ok) {
         tc_fence_after();
-        if (j + 1 < nA) issue_s(0, j + 1);
+        if (nA > 0) issue_s(0, 0);
+        if (nB > 0) issue_s(1, 0);
+        commit_if(kStages < n_kv, B_KE + 0);
+        __syncwarp();
       }
-      if (j < nB) {
-        if (!(ok = warp_wait(&bars[B_PR + 1], j & 1, abort_flag))) break;
-        tc_fence_after();
-        issue_pv(1, j);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % kStages;
+        if (!(ok = warp_wait(&bars[kReadyV + st], (j / kStages) & 1, abort_flag))) break;
+        const int zero_from = seq_len - (j0 + j) * kBN;  // V rows at or past the sequence end: exact zeros
+        if (kQ == 0 && zero_from < kBN) {  // (8-bit caches: the converters write those rows as zeros)
+          uint8_t* vbp = smem + kOffV + st * kTileBytes;
+          const int rows = kBN - zero_from;
+          for (int i = lane; i < rows * (kD / 8); i += 32) {
+            const int row = zero_from + i / (kD / 8), c = i % (kD / 8);
+            *reinterpret_cast<uint4*>(vbp + L::at(row, c >> 3) + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (j < nA) {
+          if (!(ok = warp_wait(&bars[B_PR + 0], j & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(0, j);
+        }
+        const bool next = j + 1 < n_kv;
+        if (next) {
+          if (!(ok = warp_wait(&bars[kReadyK + (j + 1) % kStages], ((j + 1) / kStages) & 1, abort_flag))) break;
+          tc_fence_after();
+          if (j + 1 < nA) issue_s(0, j + 1);
+        }
+        if (j < nB) {
+          if (!(ok = warp_wait(&bars[B_PR + 1], j & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(1, j);
+        }
+        // release V_j, then issue S_B(j+1) and release K_{j+1}, each only if the producer will
+        // refill that stage (an arrive nobody waits for could land after this CTA has left)
+        commit_if(j + kStages < n_kv, B_VE + st);
+        if (next) {
+          if (j + 1 < nB) issue_s(1, j + 1);
+          commit_if(j + 1 + kStages < n_kv, B_KE + (j + 1) % kStages);
+        }
+        __syncwarp();
       }
-      // release V_j, then issue S_B(j+1) and release K_{j+1}, each only if the producer will
-      // refill that stage (an arrive nobody waits for could land after this CTA has left)
-      commit_if(j + kStages < n_kv, B_VE + st);
-      if (next) {
-        if (j + 1 < nB) issue_s(1, j + 1);
-        commit_if(j + 1 + kStages < n_kv, B_KE + (j + 1) % kStages);
-      }
-      __syncwarp();
+      if (!ok) set_abort(abort_flag, p.err);
     }
-    if (!ok) set_abort(abort_flag, p.err);
   } else if (kQ != 0 && warp >= 10) {
     // ------------------------------------------------ 8-bit caches: warps 10-11 dequantise each
     // K and V tile in place ("32. Production attention kernels", Quantized KV caches: the tile of
@@ -523,10 +621,12 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     if (!ok) set_abort(abort_flag, p.err);
   } else {
     // ------------------------------------------------ softmax: warps 0-3 tile A, 4-7 tile B
+    // (a lone tile: both groups on tile A's rows, group t taking key tiles t, t + 2, ... into
+    // O block t; group 0 merges the two at the end)
     const int t = warp >> 2;
-    const int n_mine = t == 0 ? nA : nB;
+    const int n_mine = lone ? (nA + 1 - t) / 2 : (t == 0 ? nA : nB);
     const int row = tid & (kBM - 1);
-    const int tok = tok0 + t * TOK + row / G;
+    const int tok = tok0 + (lone ? 0 : t) * TOK + row / G;
     const bool row_valid = tok < q_len;
     const int qpos = seq_len - q_len + tok;
     const int vis_end = p.causal ? min(qpos + 1, seq_len) : seq_len;
@@ -536,12 +636,15 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + col_s(t);
     const uint32_t o_col = lane_base + col_o<kD>(t);
-    // a sink logit starts the running state: it joins the denominator and adds no value
-    float m_run = p.sinks != nullptr ? p.sinks[kvh * G + row % G] * kLog2e : -INFINITY;
-    float l_run = p.sinks != nullptr ? 1.f : 0.f;
+    // a sink logit starts the running state: it joins the denominator and adds no value (a lone
+    // tile: in group 0's state only)
+    const bool sink = p.sinks != nullptr && !(lone && t == 1);
+    float m_run = sink ? p.sinks[kvh * G + row % G] * kLog2e : -INFINITY;
+    float l_run = sink ? 1.f : 0.f;
     bool ok = true;
-    for (int j = 0; j < n_mine; ++j) {
-      if (!warp_wait(&bars[B_SF + t], j & 1, abort_flag)) {
+    for (int k = 0; k < n_mine; ++k) {
+      const int j = lone ? 2 * k + t : k;  // the key tile (counted from j0)
+      if (!warp_wait(&bars[B_SF + t], k & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -579,7 +682,7 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       if (m_run == -INFINITY || mxs > m_run + kRescaleThreshold) {
         m_new = mxs;
         alpha = exp2f(m_run - (m_new == -INFINITY ? 0.f : m_new));
-        rescale = (j > 0);
+        rescale = (k > 0);
       }
       const float mu = (m_new == -INFINITY) ? 0.f : m_new;
       // probabilities, packed to bf16 pairs over the score columns already consumed
@@ -613,7 +716,7 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       const float lsum = la + lb;
       l_run = l_run * alpha + lsum;
       m_run = m_new;
-      // S_t(j) has landed, so P.V of tile j-1 (issued before it) is complete: O is stable
+      // this S has landed, so the P.V into O_t before it (issued earlier) is complete: O is stable
       if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? alpha : 1.f;
 #pragma unroll
@@ -630,7 +733,24 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars[B_PR + t]);
     }
+    // the last P.V of this tile
     if (ok && n_mine > 0 && !warp_wait(&bars[B_OD + t], (n_mine - 1) & 1, abort_flag)) ok = false;
+    // a lone tile of two or more key tiles: group 1 hands its rows' (m, l) to group 0, which merges
+    // O block 1 into its own. Group 1's last P.V was issued after every S, so K stage 0 is free.
+    const bool merge = lone && nA > 1;
+    float m_o = -INFINITY, l_o = 0.f;
+    if (merge) {
+      float* xch = reinterpret_cast<float*>(smem + L::k_stage(0));
+      if (t == 1) {
+        xch[row] = m_run;
+        xch[kBM + row] = l_run;
+        asm volatile("bar.arrive 2, 256;" ::: "memory");
+      } else {
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        m_o = xch[row];
+        l_o = xch[kBM + row];
+      }
+    }
     if (!ok) {
       set_abort(abort_flag, p.err);
     } else if (kPrefix) {
@@ -657,24 +777,44 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
           p.ws_ml[slot * 2 + 1] = l_run;
         }
       }
-    } else if (n_mine > 0) {
+    } else if (n_mine > 0 && !(lone && t == 1)) {
       tc_fence_after();
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      // O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)), m the larger
+      float a0 = 1.f, a1 = 0.f, l = l_run;
+      if (merge) {
+        const float m = fmaxf(m_run, m_o);
+        const float mu = m == -INFINITY ? 0.f : m;
+        a0 = exp2f(m_run - mu);
+        a1 = exp2f(m_o - mu);
+        l = l_run * a0 + l_o * a1;
+      }
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float s0 = a0 * inv, s1 = a1 * inv;
+      const uint32_t o1_col = lane_base + col_o<kD>(1);
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)(q_start + tok) * p.out_stride +
                            (size_t)(kvh * G + row % G) * kD;
 #pragma unroll
       for (int q4 = 0; q4 < kD / 32; ++q4) {
         uint32_t ov[32];
+        float o[32];
         tmem_ld32(o_col + 32 * q4, ov);
         tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(ov[i]) * s0;
+        if (merge) {
+          tmem_ld32(o1_col + 32 * q4, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = fmaf(__uint_as_float(ov[i]), s1, o[i]);
+        }
         if (row_valid) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+            w.x = pack_bf16x2(o[i], o[i + 1]);
+            w.y = pack_bf16x2(o[i + 2], o[i + 3]);
+            w.z = pack_bf16x2(o[i + 4], o[i + 5]);
+            w.w = pack_bf16x2(o[i + 6], o[i + 7]);
             *reinterpret_cast<uint4*>(out + q4 * 32 + i) = w;
           }
         }
@@ -693,9 +833,9 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     if (warp == 8 && lane == 0) {
       (void)mbar_wait(&bars[B_Q], 0);
       const int issued = *issued_tiles;
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
-        (void)mbar_wait(&bars[B_KF + j % kStages], (j / kStages) & 1);
-        (void)mbar_wait(&bars[B_VF + j % kStages], (j / kStages) & 1);
+      for (int j = max(0, issued - n_stages); j < issued; ++j) {
+        (void)mbar_wait(&bars[B_KF + j % n_stages], (j / n_stages) & 1);
+        (void)mbar_wait(&bars[B_VF + j % n_stages], (j / n_stages) & 1);
       }
     }
     __syncthreads();

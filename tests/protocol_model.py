@@ -246,3 +246,102 @@ def varlen_pair(nA: int, nB: int, seed: int, stages: int = 2, conditional_releas
                 raise ProtocolError(f"O_{t} read before its last P.V landed")
 
     m.run({"producer": producer(), "mma": mma(), "softmaxA": softmax(0), "softmaxB": softmax(1)})
+
+
+# ------------------------------------------------------------------ varlen lone tile
+def varlen_lone(nA: int, seed: int, stages: int = 3, merge_wait: bool = True):
+    """One CTA whose second query tile is empty: a `stages`-deep K and V ring; the two softmax
+    groups take the key tiles in turn (tile j: group j % 2, score block j % 2, O block j % 2); the
+    MMA issue order S(0), S(1), then per key tile P.V(j), S(j+2). At the end group 1 hands its
+    row state to group 0 through K stage 0 (a named barrier) and group 0 merges O block 1 into
+    its own (merge_wait: group 0 waits at the named barrier first)."""
+    m = Machine(seed)
+    for name in ["Q", "NB"] + [f"{x}{s}" for x in ("KF", "VF", "KE", "VE") for s in range(stages)] + \
+            [f"{x}{b}" for x in ("SF", "PR", "OD") for b in range(2)]:
+        m.bar(name)
+    state = {"stage_readers": {}, "content": {}, "softmax_in": [False, False], "p_readers": [0, 0],
+             "pv_left": [0, 0], "handed": False}
+
+    def producer():
+        m.copy("Q")
+        for i in range(nA):
+            st = i % stages
+            for x, rel in (("K", "KE"), ("V", "VE")):
+                if i >= stages:
+                    yield wait(f"{rel}{st}", i // stages - 1)
+                if state["stage_readers"].get((x, st), 0):
+                    raise ProtocolError(f"{x} stage {st} refilled while the tensor pipe reads it")
+                if x == "K" and st == 0 and state["handed"]:
+                    raise ProtocolError("K stage 0 refilled after the hand-over wrote it")
+                state["content"][(x, st)] = i
+                m.copy(f"{x}F{st}")
+
+    def issue(kind, tile):
+        key, b = ("K" if kind == "S" else "V", tile % stages), tile & 1
+        if state["content"].get(key) != tile:
+            raise ProtocolError(f"{kind} of tile {tile} issued on stage holding {state['content'].get(key)}")
+        state["stage_readers"][key] = state["stage_readers"].get(key, 0) + 1
+        if kind == "PV":
+            state["pv_left"][b] += 1
+            state["p_readers"][b] += 1
+
+        def done():
+            if state["content"].get(key) != tile:
+                raise ProtocolError(f"{kind} of tile {tile} read a refilled stage")
+            if key == ("K", 0) and state["handed"]:
+                raise ProtocolError("S read K stage 0 after the hand-over wrote it")
+            state["stage_readers"][key] -= 1
+            if kind == "S":
+                if state["softmax_in"][b] or state["p_readers"][b]:
+                    raise ProtocolError(f"score block {b} overwritten while it is still read")
+            else:
+                state["pv_left"][b] -= 1
+                state["p_readers"][b] -= 1
+        m.op(done)
+        m.commit(f"SF{b}" if kind == "S" else f"OD{b}")
+        if kind == "S" and tile + stages < nA:
+            m.commit(f"KE{tile % stages}")
+
+    def mma():
+        yield wait("Q", 0)
+        for j in range(min(2, nA)):
+            yield wait(f"KF{j}", 0)
+            issue("S", j)
+        for j in range(nA):
+            st = j % stages
+            yield wait(f"VF{st}", j // stages)
+            yield wait(f"PR{j & 1}", j >> 1)
+            issue("PV", j)
+            if j + stages < nA:
+                m.commit(f"VE{st}")
+            if j + 2 < nA:
+                yield wait(f"KF{(j + 2) % stages}", (j + 2) // stages)
+                issue("S", j + 2)
+
+    def softmax(t):
+        n_mine = (nA + 1 - t) // 2
+        for k in range(n_mine):
+            yield wait(f"SF{t}", k)
+            state["softmax_in"][t] = True
+            yield STEP
+            if k > 0 and state["pv_left"][t]:  # O_t rescaled (in the worst case, every tile)
+                raise ProtocolError(f"O_{t} rescaled while a P.V still accumulates into it")
+            state["softmax_in"][t] = False
+            m.bars[f"PR{t}"].arrive()
+        if n_mine:
+            yield wait(f"OD{t}", n_mine - 1)
+            if state["pv_left"][t]:
+                raise ProtocolError(f"O_{t} read before its last P.V landed")
+        if nA > 1:
+            if t == 1:
+                if state["stage_readers"].get(("K", 0), 0) or any(b == "KF0" for b, _ in m.copies):
+                    raise ProtocolError("the hand-over wrote K stage 0 while it is still in use")
+                state["handed"] = True
+                m.bars["NB"].arrive()
+            else:
+                if merge_wait:
+                    yield wait("NB", 0)
+                if not state["handed"] or state["pv_left"][1]:
+                    raise ProtocolError("group 0 merged before group 1's state and O block were final")
+
+    m.run({"producer": producer(), "mma": mma(), "softmax0": softmax(0), "softmax1": softmax(1)})

@@ -7,7 +7,7 @@ import random
 
 import pytest
 
-from protocol_model import ProtocolError, decode_ring, varlen_pair
+from protocol_model import ProtocolError, decode_ring, varlen_lone, varlen_pair
 
 # the decode kernel's rings: (stages, producer warps, consumer warps, early release)
 DECODE_RINGS = [(8, 2, 4, False),   # bf16, head_dim 128: 8 stages of 8 KiB
@@ -32,6 +32,12 @@ def test_varlen_pair_protocol():
     for trial, (nA, nB) in enumerate(cases):
         for seed in range(25):
             varlen_pair(nA, nB, seed=trial * 1000 + seed)
+
+
+def test_varlen_lone_protocol():
+    for nA in list(range(1, 12)) + [17, 32]:
+        for seed in range(40):
+            varlen_lone(nA, seed=nA * 1000 + seed)
 
 
 def _caught(fn, *args, **kw):
@@ -61,3 +67,8 @@ def test_model_catches_a_release_nobody_waits_for():
 
 def test_model_catches_a_wrong_score_phase():
     assert _caught(varlen_pair, 4, 4, score_phase_offset=1)
+
+
+def test_model_catches_a_lone_tile_merging_without_the_named_barrier():
+    assert _caught(varlen_lone, 6, merge_wait=False)
+
