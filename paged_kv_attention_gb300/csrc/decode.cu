@@ -143,13 +143,13 @@ __global__ void __launch_bounds__(DecCfg<D, QK>::kThreads)
           if (!page_ok) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // TMA reads zeros
           uint8_t* st = smem + stage * C::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-#pragma unroll
-          for (int a = 0; a < C::kBoxes; ++a)
-            tma_load_4d(st + a * (kChunk * 128), &kmap, &full[stage], a * (128 / C::kElt), kvh, in_page, page);
-#pragma unroll
-          for (int a = 0; a < C::kBoxes; ++a)
-            tma_load_4d(st + C::kTileBytes + a * (kChunk * 128), &vmap, &full[stage], a * (128 / C::kElt), kvh,
-                        in_page, page);
+          if constexpr (C::kBoxes > 1) {  // every 128-byte column of the chunk in one copy (5-D map)
+            tma_load_5d(st, &kmap, &full[stage], 0, in_page, 0, kvh, page);
+            tma_load_5d(st + C::kTileBytes, &vmap, &full[stage], 0, in_page, 0, kvh, page);
+          } else {
+            tma_load_4d(st, &kmap, &full[stage], 0, kvh, in_page, page);
+            tma_load_4d(st + C::kTileBytes, &vmap, &full[stage], 0, kvh, in_page, page);
+          }
         }
         issued = i + 1;
       }

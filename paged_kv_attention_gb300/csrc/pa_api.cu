@@ -72,6 +72,27 @@ bool encode_cache_map_pages(CUtensorMap* map, const void* base, int D, int Hkv, 
   return r == CUDA_SUCCESS;
 }
 
+// The split-KV decode's K / V maps: one box is `box_tokens` rows of one KV head over every
+// 128-byte column of the row, landing as [column][row][128 bytes] (the 4-D map's boxes, one copy
+// instead of one per column). The pool viewed as (128-byte columns' elements, bs, columns, Hkv,
+// blocks).
+bool encode_decode_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, int bs, int num_blocks,
+                             int box_tokens, int elt = 2) {
+  const int cols = D * elt / 128;
+  if (cols <= 1) return encode_cache_map(map, base, D, Hkv, bs, num_blocks, box_tokens, elt);
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[5] = {(cuuint64_t)(128 / elt), (cuuint64_t)bs, (cuuint64_t)cols, (cuuint64_t)Hkv,
+                        (cuuint64_t)num_blocks};
+  cuuint64_t strides[4] = {(cuuint64_t)Hkv * D * elt, 128, (cuuint64_t)D * elt, (cuuint64_t)bs * Hkv * D * elt};
+  cuuint32_t box[5] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_tokens, (cuuint32_t)cols, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // The bf16 K / V maps of the tensor-core varlen kernels: whole-page boxes at head_dim 128, one
 // box per page and 64-column block otherwise (head_dim 64 has one block; the head_dim-256 kernel
 // keeps its own layout).
@@ -379,8 +400,8 @@ pa_status run_decode_units(DecodeParams& p, pa_dtype dtype, const void* k_cache,
   if (dtype == PA_DTYPE_BF16 || p.quant != 0) {
     const int elt = p.quant != 0 ? 1 : 2;
     CUtensorMap kmap, vmap;
-    if (!encode_cache_map(&kmap, k_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk, elt) ||
-        !encode_cache_map(&vmap, v_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk, elt))
+    if (!encode_decode_cache_map(&kmap, k_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk, elt) ||
+        !encode_decode_cache_map(&vmap, v_cache, D, p.num_kv_heads, p.block_size, p.num_blocks, kChunk, elt))
       return PA_ERR_CUDA;
     e = launch_decode_bf16(p, kmap, vmap, stream);
   } else {
@@ -1188,8 +1209,8 @@ extern "C" pa_status pa_cascade_decode(const void* q, const void* k_cache, const
   // pass leaves free, while it runs (they finish only after it, for the combine's sake)
   p.overlap_previous = 1;
   CUtensorMap skmap, svmap;
-  if (!encode_cache_map(&skmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk) ||
-      !encode_cache_map(&svmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk))
+  if (!encode_decode_cache_map(&skmap, k_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk) ||
+      !encode_decode_cache_map(&svmap, v_cache, head_dim, num_kv_heads, block_size, num_blocks, kChunk))
     return PA_ERR_CUDA;
   if (launch_decode_bf16(p, skmap, svmap, strm) != cudaSuccess) return PA_ERR_CUDA;
 
