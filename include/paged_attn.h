@@ -305,8 +305,8 @@ pa_status pa_paged_attention_varlen_strided(const void* q, const void* k_cache, 
 /* Where a varlen call with a workspace runs the batch's short requests (1 to 8 queries:
  * decodes and speculative verify blocks). */
 typedef enum {
-  PA_SHORT_AUTO = 0,   /* the split-KV decode for a batch of many short requests (num_reqs >= 64
-                          and num_tokens <= 32 * num_reqs), else the tensor-core kernel (its decode
+  PA_SHORT_AUTO = 0,   /* the split-KV decode for a batch of many short requests (num_reqs >= 80
+                          and num_tokens <= 8 * num_reqs), else the tensor-core kernel (its decode
                           tiles then run beside the prefill tiles from the start; the split path's
                           extra launches only pay off over many short requests) */
   PA_SHORT_SPLIT = 1,  /* always the split-KV decode */

@@ -219,7 +219,7 @@ def paged_attention_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     "auto", "split" or "tensor" run the tensor-core kernel on a grid planned on the device (only
     the tile pairs the batch has, longest first; graph-safe), with the short requests (1 to 8
     queries) on the split-KV decode for "split", on the tensor-core kernel for "tensor", and for
-    "auto" on the split-KV decode when the batch has >= 64 requests averaging <= 32 queries.
+    "auto" on the split-KV decode when the batch has >= 80 requests averaging <= 8 queries.
     Without ``schedule``: ``work_items`` (a host plan, see varlen_plan) or the default grid, with
     ``split_decodes`` sending the short requests to the split-KV decode."""
     n, hq, d = q.shape

@@ -664,12 +664,14 @@ namespace {
 // kAutoSplitMinReqs requests averaging at most kAutoSplitMaxAvgQueries queries. The split path adds
 // a launch chain (plan, tensor-core grid, decode, combine: ~10 us) that only many short requests
 // repay, while on the tensor-core grid decode tiles run beside the prefill tiles from the start.
-// Measured on GB300 (us, planned tensor-core grid vs split, L2 cold): 8 prefill chunks of 512 + 48
-// decodes + 8 verify blocks 186 vs 205; 48 decodes + 8 verify blocks 111 vs 119; 2 chunks + 48
-// decodes + 8 verify 136 vs 146; 48 decodes 99 vs 99; 1 chunk + 64 decodes 121 vs 118; 4 chunks +
-// 128 decodes 260 vs 254; 256 decodes 420 vs 358.
-constexpr int kAutoSplitMinReqs = 64;
-constexpr int kAutoSplitMaxAvgQueries = 32;
+// Measured on GB300 (us, device-planned tensor-core grid vs split, L2 cold; contexts up to 4,096,
+// chunks of 512, verify blocks of 5): 8 chunks + 48 decodes + 8 verify blocks 182 vs 203; 48
+// decodes + 8 verify 103 vs 113; 2 chunks + 48 decodes + 8 verify 132 vs 142; 1 chunk + 64
+// decodes 115 vs 117; 4 chunks + 128 decodes 250 vs 252; 48 decodes 91 vs 95; 64 decodes 108 vs
+// 110; 96 decodes 149 vs 145; 128 decodes 203 vs 189; 120 decodes + 8 verify 205 vs 194; 1 chunk +
+// 256 decodes 396 vs 373; 256 decodes 404 vs 353; 512 decodes 744 vs 630.
+constexpr int kAutoSplitMinReqs = 80;
+constexpr int kAutoSplitMaxAvgQueries = 8;
 
 pa_status varlen_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
                       const int32_t* seq_lens, const int32_t* block_tables, int num_reqs, int num_tokens,

@@ -395,16 +395,16 @@ def test_device_planned_grid_follows_the_batch_under_graph_replay(hq, hkv, bs):
 def test_schedules(hq, hkv, bs):
     """pa_paged_attention_varlen_sched: "tensor" (device-planned grid, every request on the tensor
     cores) equals the default grid bit for bit; "split" equals the split path; "auto" picks the
-    split-KV decode for a batch of many short requests (>= 64 requests, <= 32 queries each on
+    split-KV decode for a batch of many short requests (>= 80 requests, <= 8 queries each on
     average) and the tensor-core kernel otherwise; all agree with the oracle."""
     heavy = workloads.make_case("vsch", 3200 + hq + bs, [300, 1, 5, 130, 1, 64], [900, 3000, 1100, 130, 17, 2500],
                                 num_q_heads=hq, num_kv_heads=hkv, head_dim=128, block_size=bs, dtype=torch.bfloat16)
     gen = torch.Generator().manual_seed(3300 + hq + bs)
-    lq = [1, 5, 2, 1, 8, 3] * 11 + [100]
+    lq = [1, 5, 2, 1, 8, 3] * 14 + [20]
     ls = [int(x) for x in torch.randint(120, 1500, (len(lq),), generator=gen)]
     light = workloads.make_case("vsch", 3300 + hq + bs, lq, ls, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
                                 block_size=bs, dtype=torch.bfloat16)
-    assert heavy.num_reqs < 64 and light.num_reqs >= 64 and light.num_tokens <= 32 * light.num_reqs
+    assert heavy.num_reqs < 80 and light.num_reqs >= 80 and light.num_tokens <= 8 * light.num_reqs
     for case in (heavy, light):
         kc, vc = gpu_pools(case)
         ko, vo = oracle_pools(case)
