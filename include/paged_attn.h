@@ -203,9 +203,10 @@ pa_status pa_paged_attention_decode(const void* q, const void* k_cache, const vo
  *   max_blocks_per_seq * block_size, gets zero rows and a flag.
  * Supported: D in {64, 128, 256}; bf16 with Hq/Hkv <= 16 and block_size % 16 == 0 (the
  *   tcgen05 tensor-core kernels serve every D with Hq/Hkv in {1,2,4,8,16} and block_size in
- *   {16,32,64,128}: at D 64 and 128 a CTA's two query tiles share each K/V tile, at D 256 it
- *   runs them one after the other; other bf16 shapes run every query token as a one-split
- *   decode); f32 with (Hq/Hkv) * D <= 2048 and any block_size. */
+ *   {16,32,64,128}: at D 64 and 128 a CTA's two query tiles share each K/V tile, and a CTA
+ *   whose second tile is empty (decodes, verify blocks) splits its key tiles between its two
+ *   softmax groups; at D 256 it runs the two tiles one after the other; other bf16 shapes run
+ *   every query token as a one-split decode); f32 with (Hq/Hkv) * D <= 2048 and any block_size. */
 pa_status pa_paged_attention_varlen(const void* q, const void* k_cache, const void* v_cache,
                                     const int32_t* query_start_loc, const int32_t* seq_lens,
                                     const int32_t* block_tables,

@@ -431,3 +431,26 @@ def test_split_schedule_without_workspace_is_refused():
         case.num_blocks, case.block_tables.shape[1], 1, 0.0, pa._lib.PA_DTYPE_BF16, out.data_ptr(), None, None,
         pa._lib.PA_SHORT_SPLIT, None, 0, None, None)
     assert st == pa._lib.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+# Lone query tiles: a pair whose second tile is empty splits its key tiles between the two softmax
+# groups (even tiles one group, odd tiles the other) over a three-stage K/V ring, and merges the two
+# partial states at the end. Key-tile counts 1 to 9 and 33 cover the single-group case, the ring's
+# wrap at every phase, and the merge; 2 * TOK + 5 queries give a full pair followed by a lone one.
+@pytest.mark.parametrize("head_dim,hq,hkv,bs", [(128, 32, 8, 16), (128, 16, 1, 128), (64, 16, 2, 32),
+                                                (128, 64, 4, 64)])
+@pytest.mark.parametrize("window,softcap,sinks", [(0, 0.0, False), (150, 25.0, True)])
+def test_lone_tiles(head_dim, hq, hkv, bs, window, softcap, sinks):
+    tok = 128 // (hq // hkv)
+    keys = [1, 128, 129, 256, 300, 384, 513, 640, 900, 1152, 4200]
+    q_lens = [1, tok, 5, 1, tok - 1, 3, 1, tok, 2, 7, 1] + [2 * tok + 5]
+    seq_lens = keys + [1500]
+    case = workloads.make_case("vlone", 7100 + head_dim + hq + bs, q_lens, seq_lens, num_q_heads=hq,
+                               num_kv_heads=hkv, head_dim=head_dim, block_size=bs, dtype=torch.bfloat16)
+    kc, vc = gpu_pools(case)
+    ko, vo = oracle_pools(case)
+    sk = torch.linspace(-1.0, 2.5, hq, dtype=torch.float32) if sinks else None
+    out = run_varlen(case, kc, vc, window=window, softcap=softcap, sinks=None if sk is None else sk.to(DEV))
+    want = oracle.paged_attention_varlen(case.q, ko, vo, case.query_start_loc, case.seq_lens, case.block_tables,
+                                         True, case.scale, window=window, softcap=softcap, sinks=sk)
+    check_close(out, want, torch.bfloat16, label=f"lone D{head_dim} G{hq // hkv} bs{bs} w{window}")
