@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* issued_tiles = reinterpret_cast<int*>(tmem_slot + 2);
+  int* issued_k = reinterpret_cast<int*>(tmem_slot + 2);  // K / V tiles whose copies are out
+  int* issued_v = reinterpret_cast<int*>(tmem_slot + 3);
 
   // ---- which tile pair: from the caller's plan (heaviest first by the host's estimate, no empty
   // pairs), else heaviest (last) query tiles first across all requests and heads
@@ -321,7 +322,8 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     mbar_init(&bars[B_FIN], 1);
     fence_barrier_init();
     *abort_flag = 0;
-    *issued_tiles = 0;
+    *issued_k = 0;
+    *issued_v = 0;
   }
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -374,64 +376,49 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
     };
     float* scales = reinterpret_cast<float*>(smem + kOffScale);  // [stage][K 128 | V 128]
-    int cur = n_kv > 0 ? page_of(0) : 0;
-    for (int i = 0; i < n_kv; ++i) {
+    // Copies of tile i go to stage i % n_stages once the tensor core has released the stage's
+    // previous tile. A lone tile's K copies run one tile ahead of its V copies: a V stage frees
+    // only after its P.V, and K(i + 1) would otherwise wait behind V(i) for it.
+    const int lead = lone ? 1 : 0;
+    auto copy_tile = [&](bool is_v, int i, int page) -> bool {
       const int st = i % n_stages;
-      const uint32_t round_parity = ((i / n_stages) - 1) & 1;
       const int p0 = (j0 + i) * pages_per_tile;
       const int np = min(p0 + pages_per_tile, seq_pages) - p0;
       const uint32_t bytes = (uint32_t)np * bs * (uint32_t)(kQ != 0 ? kD : kD * 2);
-      const int nxt = i + 1 < n_kv ? page_of(i + 1) : 0;
-      if (i >= n_stages && !warp_wait(&bars[B_KE + st], round_parity, abort_flag)) {
+      uint64_t* full = &bars[(is_v ? B_VF : B_KF) + st];
+      if (i >= n_stages && !warp_wait(&bars[(is_v ? B_VE : B_KE) + st], ((i / n_stages) - 1) & 1, abort_flag))
+        return false;
+      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+      __syncwarp();
+      uint8_t* dst = smem + (is_v ? L::v_stage(st) : L::k_stage(st));
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      if (lane < np) {
+        if (!is_v && (page < 0 || page >= p.num_blocks)) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
+        if constexpr (kQ != 0) {  // the page's codes: one 128-byte row per key, into column block 1
+          tma_load_4d(dst + kRegion + lane * bs * 128, map, full, 0, kvh, 0, page);
+        } else if constexpr (L::kWide) {  // the whole page (bs / 8 row groups) in one copy
+          tma_load_5d(dst + L::at(lane * bs, 0), map, full, 0, 0, 0, page * (bs / 8), kvh);
+        } else {
+          for (int a = 0; a < kBlocks; ++a) tma_load_4d(dst + a * kRegion + lane * bs * 128, map, full, a * 64, kvh, 0, page);
+        }
+      }
+      if constexpr (kQ != 0) copy_scales(i, st, page, is_v ? p.v_scales : p.k_scales, is_v ? scales + 128 : scales, full);
+      __syncwarp();
+      if (lane == 0) *(is_v ? issued_v : issued_k) = i + 1;
+      return true;
+    };
+    int cur = n_kv > 0 ? page_of(0) : 0, prev = 0;  // this lane's page of tile e, of tile e - 1
+    for (int e = 0; e < n_kv + lead; ++e) {
+      const int nxt = e + 1 < n_kv ? page_of(e + 1) : 0;
+      if (e < n_kv && !copy_tile(false, e, cur)) {
         if (lane == 0) set_abort(abort_flag, p.err);
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars[B_KF + st], bytes);
-      __syncwarp();
-      if (lane < np) {
-        if (cur < 0 || cur >= p.num_blocks) flag_error(p.err, PA_ERRBIT_PAGE_OUT_OF_POOL);  // reads zeros
-        if constexpr (kQ != 0) {  // the page's codes: one 128-byte row per key, into column block 1
-          tma_load_4d(smem + L::k_stage(st) + kRegion + lane * bs * 128, &kmap, &bars[B_KF + st], 0, kvh, 0,
-                      cur);
-        } else {
-          if constexpr (L::kWide) {  // the whole page (bs / 8 row groups) in one copy
-            tma_load_5d(smem + L::k_stage(st) + L::at(lane * bs, 0), &kmap, &bars[B_KF + st], 0, 0, 0, cur * (bs / 8),
-                        kvh);
-          } else {
-            for (int a = 0; a < kBlocks; ++a)
-              tma_load_4d(smem + L::k_stage(st) + a * kRegion + lane * bs * 128, &kmap, &bars[B_KF + st], a * 64,
-                          kvh, 0, cur);
-          }
-        }
-      }
-      if constexpr (kQ != 0) copy_scales(i, st, cur, p.k_scales, scales, &bars[B_KF + st]);
-      if (i >= n_stages && !warp_wait(&bars[B_VE + st], round_parity, abort_flag)) {
-        if (lane == 0) {
-          set_abort(abort_flag, p.err);
-          *issued_tiles = i + 1;  // K of iteration i is in flight
-        }
+      if (e - lead >= 0 && !copy_tile(true, e - lead, lead ? prev : cur)) {
+        if (lane == 0) set_abort(abort_flag, p.err);
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars[B_VF + st], bytes);
-      __syncwarp();
-      if (lane < np) {
-        if constexpr (kQ != 0) {
-          tma_load_4d(smem + L::v_stage(st) + kRegion + lane * bs * 128, &vmap, &bars[B_VF + st], 0, kvh, 0,
-                      cur);
-        } else {
-          if constexpr (L::kWide) {  // the whole page (bs / 8 row groups) in one copy
-            tma_load_5d(smem + L::v_stage(st) + L::at(lane * bs, 0), &vmap, &bars[B_VF + st], 0, 0, 0, cur * (bs / 8),
-                        kvh);
-          } else {
-            for (int a = 0; a < kBlocks; ++a)
-              tma_load_4d(smem + L::v_stage(st) + a * kRegion + lane * bs * 128, &vmap, &bars[B_VF + st], a * 64,
-                          kvh, 0, cur);
-          }
-        }
-      }
-      if constexpr (kQ != 0) copy_scales(i, st, cur, p.v_scales, scales + 128, &bars[B_VF + st]);
-      __syncwarp();
-      if (lane == 0) *issued_tiles = i + 1;
+      prev = cur;
       cur = nxt;
     }
   } else if (warp == 9) {
@@ -832,11 +819,9 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
     }
     if (warp == 8 && lane == 0) {
       (void)mbar_wait(&bars[B_Q], 0);
-      const int issued = *issued_tiles;
-      for (int j = max(0, issued - n_stages); j < issued; ++j) {
-        (void)mbar_wait(&bars[B_KF + j % n_stages], (j / n_stages) & 1);
-        (void)mbar_wait(&bars[B_VF + j % n_stages], (j / n_stages) & 1);
-      }
+      const int ik = *issued_k, iv = *issued_v;
+      for (int j = max(0, ik - n_stages); j < ik; ++j) (void)mbar_wait(&bars[B_KF + j % n_stages], (j / n_stages) & 1);
+      for (int j = max(0, iv - n_stages); j < iv; ++j) (void)mbar_wait(&bars[B_VF + j % n_stages], (j / n_stages) & 1);
     }
     __syncthreads();
   }

@@ -249,12 +249,13 @@ def varlen_pair(nA: int, nB: int, seed: int, stages: int = 2, conditional_releas
 
 
 # ------------------------------------------------------------------ varlen lone tile
-def varlen_lone(nA: int, seed: int, stages: int = 3, merge_wait: bool = True):
+def varlen_lone(nA: int, seed: int, stages: int = 3, merge_wait: bool = True, lead: int = 1):
     """One CTA whose second query tile is empty: a `stages`-deep K and V ring; the two softmax
     groups take the key tiles in turn (tile j: group j % 2, score block j % 2, O block j % 2); the
     MMA issue order S(0), S(1), then per key tile P.V(j), S(j+2). At the end group 1 hands its
     row state to group 0 through K stage 0 (a named barrier) and group 0 merges O block 1 into
-    its own (merge_wait: group 0 waits at the named barrier first)."""
+    its own (merge_wait: group 0 waits at the named barrier first). The producer's K copies run
+    `lead` tiles ahead of its V copies."""
     m = Machine(seed)
     for name in ["Q", "NB"] + [f"{x}{s}" for x in ("KF", "VF", "KE", "VE") for s in range(stages)] + \
             [f"{x}{b}" for x in ("SF", "PR", "OD") for b in range(2)]:
@@ -264,9 +265,11 @@ def varlen_lone(nA: int, seed: int, stages: int = 3, merge_wait: bool = True):
 
     def producer():
         m.copy("Q")
-        for i in range(nA):
-            st = i % stages
-            for x, rel in (("K", "KE"), ("V", "VE")):
+        for e in range(nA + lead):
+            for x, rel, i in (("K", "KE", e), ("V", "VE", e - lead)):
+                if not 0 <= i < nA:
+                    continue
+                st = i % stages
                 if i >= stages:
                     yield wait(f"{rel}{st}", i // stages - 1)
                 if state["stage_readers"].get((x, st), 0):

@@ -34,10 +34,12 @@ def test_varlen_pair_protocol():
             varlen_pair(nA, nB, seed=trial * 1000 + seed)
 
 
-def test_varlen_lone_protocol():
+@pytest.mark.parametrize("lead", [0, 1])
+def test_varlen_lone_protocol(lead):
+    # lead 1: the kernel's order, K copies one tile ahead of V copies; lead 0 also holds
     for nA in list(range(1, 12)) + [17, 32]:
         for seed in range(40):
-            varlen_lone(nA, seed=nA * 1000 + seed)
+            varlen_lone(nA, seed=nA * 1000 + seed, lead=lead)
 
 
 def _caught(fn, *args, **kw):
