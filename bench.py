@@ -21,6 +21,7 @@ bounded sample of the same workload and prints the same metric.
 from __future__ import annotations
 
 import argparse
+import functools
 import json
 import os
 import statistics
@@ -398,29 +399,96 @@ def decode_leg(args, world, rank, dev):
         return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
                     call_reps=n_rep, call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=None,
                     h2d=0, d2h=0, launches=args.steps * (2 + (1 if splits > 1 else 0)), out=out.cpu())
-    # end to end: host buffers in (one pinned buffer, one copy), the same two calls, the host
-    # result out, all inside the timed region
+    # End to end: every step's inputs copied in from one pinned host buffer (one copy), the same
+    # two calls, every step's output read back to pinned host memory, all inside the timed
+    # region. As a serving loop runs it: two sets of device buffers, the copy-in of step i + 1
+    # (on its own stream) overlapping step i, and the read-back of step i (on a third stream)
+    # overlapping step i + 1. Each step's graph starts once its inputs have landed, and a buffer
+    # set is refilled only after the step before last has finished with it.
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    for _ in range(max(3, args.warmup // 4)):
-        din.copy_(hin, non_blocking=True)
-        run_step()
-        hout.copy_(out, non_blocking=True)
+    sets = [(din, out)]
+    views2 = []
+    din2 = torch.empty_like(din)
+    for t, v in zip(host_inputs, (q, nk, nv, ns, ctx)):
+        off = v.data_ptr() - din.data_ptr()
+        n = t.numel() * t.element_size()
+        views2.append(din2[off:off + n].view(t.dtype).view(t.shape))
+    sets.append((din2, torch.empty_like(out)))
+    step_graphs = []
+    for bi, (dbuf, obuf) in enumerate(sets):
+        qv, kv_, vv, sv, lv = (q, nk, nv, ns, ctx) if bi == 0 else views2
+        if args.no_graph:
+            step_graphs.append(functools.partial(step, qv, kv_, vv, sv, lv, obuf))
+        else:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(qv, kv_, vv, sv, lv, obuf)
+            step_graphs.append(g.replay)
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_steps(n):
+        landed = [torch.cuda.Event() for _ in range(2)]
+        done = [None, None]   # step finished with buffer set b
+        read = [None, None]   # read-back of set b's output finished
+        with torch.cuda.stream(h2d_stream):
+            sets[0][0].copy_(hin, non_blocking=True)
+            landed[0].record(h2d_stream)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(landed[b])
+            if read[b] is not None:
+                stream.wait_event(read[b])
+            step_graphs[b]()
+            done[b] = torch.cuda.Event()
+            done[b].record(stream)
+            if i + 1 < n:
+                nb = (i + 1) % 2
+                with torch.cuda.stream(h2d_stream):
+                    if done[nb] is not None:
+                        h2d_stream.wait_event(done[nb])
+                    sets[nb][0].copy_(hin, non_blocking=True)
+                    landed[nb] = torch.cuda.Event()
+                    landed[nb].record(h2d_stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(done[b])
+                hout.copy_(sets[b][1], non_blocking=True)
+                read[b] = torch.cuda.Event()
+                read[b].record(d2h_stream)
+        for r in read:
+            if r is not None:
+                stream.wait_event(r)
+
+    def serial_steps(n):  # the same, one step after another on one stream (no overlap)
+        for _ in range(n):
+            din.copy_(hin, non_blocking=True)
+            step_graphs[0]()
+            hout.copy_(out, non_blocking=True)
+
+    serial_steps(max(3, args.warmup // 4))
+    torch.cuda.synchronize()
+    barrier(world)
+    s_start, s_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_start.record(stream)
+    serial_steps(args.steps)
+    s_end.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(s_start.elapsed_time(s_end), world)
+    e2e_steps(max(3, args.warmup // 4))
     torch.cuda.synchronize()
     barrier(world)
     e2e_start = torch.cuda.Event(enable_timing=True)
     e2e_end = torch.cuda.Event(enable_timing=True)
     e2e_start.record(stream)
-    for i in range(args.steps):
-        din.copy_(hin, non_blocking=True)
-        run_step()
-        hout.copy_(out, non_blocking=True)
+    e2e_steps(args.steps)
     e2e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end), world)
     h2d = hin.numel()
     d2h = hout.numel() * hout.element_size()
     e2e_value = whole_job_rate(step_bytes, args.steps, e2e_ms, world) / 1e9
-    return dict(case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
+    e2e_serial = whole_job_rate(step_bytes, args.steps, serial_ms, world) / 1e9
+    return dict(e2e_serial=e2e_serial, e2e_ms_per_step=e2e_ms / args.steps, serial_ms_per_step=serial_ms / args.steps,
+                case=case, splits=splits, total_ms=total_ms, wall=wall, write_ms=write_ms, call_ms=call_ms,
                 call_reps=n_rep, call_bytes=call_bytes, step_bytes=step_bytes, value=value, e2e_value=e2e_value,
                 h2d=h2d, d2h=d2h, launches=args.steps * (2 + (1 if splits > 1 else 0)), out=hout.clone())
 
@@ -866,7 +934,14 @@ def main():
         "cache_write_ms": round(d["write_ms"], 5),
         "e2e": None if d["e2e_value"] is None else {
             "value": round(d["e2e_value"], 2), "unit": "GB/s", "h2d_bytes_per_step": d["h2d"],
-            "d2h_bytes_per_step": d["d2h"]},
+            "d2h_bytes_per_step": d["d2h"], "ms_per_step": round(d["e2e_ms_per_step"], 5),
+            "copies": "every step's inputs copied in from pinned host memory and its output read back to "
+                      "pinned host memory inside the timed region; the copy-in of step i + 1 and the read-back "
+                      "of step i overlap step i (two device buffer sets, two copy streams), as a serving loop "
+                      "runs them",
+            "serial": {"value": round(d["e2e_serial"], 2), "unit": "GB/s",
+                       "ms_per_step": round(d["serial_ms_per_step"], 5),
+                       "note": "the same steps with copy-in, step and read-back one after another on one stream"}},
         "gpu_launches": d["launches"],
         "decode_queries_per_s": round(world * case.num_reqs / (d["call_ms"] * 1e-3)),
         "clocks": clk,
