@@ -208,11 +208,19 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       return;
     }
   } else {
+    // heaviest (last) query tiles first, in chunks of 16 tile indices; within a chunk the pairs of
+    // one (request, KV head) are consecutive, so the CTAs running side by side read the same K/V
+    // tiles at about the same time and mostly from L2
+    constexpr int kChunkTiles = 16;
     const int per_tile = p.num_reqs * p.num_kv_heads;
-    tile = p.q_tiles - 1 - (int)(blockIdx.x / per_tile);
-    const int rem = (int)(blockIdx.x % per_tile);
-    r = rem / p.num_kv_heads;
-    kvh = rem - r * p.num_kv_heads;
+    const long long chunk_span = (long long)kChunkTiles * per_tile;
+    const int c = (int)(blockIdx.x / chunk_span);
+    const int in_chunk = (int)(blockIdx.x % chunk_span);
+    const int tiles_here = min(kChunkTiles, p.q_tiles - c * kChunkTiles);
+    const int combo = in_chunk / tiles_here;
+    tile = p.q_tiles - 1 - (c * kChunkTiles + in_chunk % tiles_here);
+    r = combo / p.num_kv_heads;
+    kvh = combo - r * p.num_kv_heads;
   }
   const int G = p.group;
   const int TOK = kBM / G;  // tokens per 128-row tile; a CTA covers 2 * TOK tokens
