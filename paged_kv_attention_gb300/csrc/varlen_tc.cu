@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
   } else {
     // heaviest (last) query tiles first, in chunks of 16 tile indices; within a chunk the pairs of
     // one (request, KV head) are consecutive, so the CTAs running side by side read the same K/V
-    // tiles at about the same time and mostly from L2
-    constexpr int kChunkTiles = 16;
+    // tiles at about the same time and mostly from L2 (bf16 at head dim 128; the other variants
+    // measured faster in the plain order, chunks of one tile index)
+    constexpr int kChunkTiles = (kQ == 0 && kD == 128 && !kPrefix) ? 16 : 1;
     const int per_tile = p.num_reqs * p.num_kv_heads;
     const long long chunk_span = (long long)kChunkTiles * per_tile;
     const int c = (int)(blockIdx.x / chunk_span);
