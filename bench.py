@@ -898,8 +898,13 @@ def main():
     clk = clocks.summary()
     if d is None:
         if rank == 0 and p is not None:
-            print(json.dumps({"prefill_only": True, "workload": p["case"].name, "value": round(p["tflops"], 2),
-                              "unit": "TFLOP/s", "attn_ms": round(p["attn_ms"], 4), "clocks": clk}), flush=True)
+            pc = p["case"]
+            wbytes = cache_write_bytes(pc.num_tokens, pc.num_kv_heads, pc.head_dim, 2)
+            print(json.dumps({"prefill_only": True, "workload": pc.name, "value": round(p["tflops"], 2),
+                              "unit": "TFLOP/s", "attn_ms": round(p["attn_ms"], 4),
+                              "cache_write_ms": round(p["write_ms"], 4),
+                              "cache_write_GBps": round(wbytes / (p["write_ms"] * 1e-3) / 1e9, 1),
+                              "clocks": clk}), flush=True)
         return
 
     case = d["case"]
@@ -956,6 +961,13 @@ def main():
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": round(p["tflops"] / tf_peak, 4),
                          "peak_source": peak_src, "traffic": traffic.get("varlen_kernel")},
         }
+        # the prompts' cache write (reshape_and_cache of all 32,768 rows), HBM-bound
+        pc = p["case"]
+        wbytes = cache_write_bytes(pc.num_tokens, pc.num_kv_heads, pc.head_dim, 2)
+        wgbs = wbytes / (p["write_ms"] * 1e-3) / 1e9
+        line["prefill"]["cache_write"] = {"algorithmic_bytes": wbytes, "GBps": round(wgbs, 1),
+                                          "frac_of_hbm_peak": round(wgbs / peaks["hbm_gbs"], 4),
+                                          "kernel": "reshape_and_cache_kernel"}
     for dim, pd in p_dims.items():
         tf_peak = peaks["bf16_tflops"]
         line[f"prefill_d{dim}"] = {
