@@ -753,20 +753,37 @@ __global__ void __launch_bounds__(kQ != 0 ? kThreadsQ : kThreads, 1)
       // cascade prefix pass: the row's unnormalised partial (acc, m in log2 units, l) in the
       // split-partial layout the combine merges. (A tile without keys here has no valid rows:
       // ranges past the prefix end left the kernel at the top.)
+      // The accumulator rows go out through this tile's Q buffer (every S of the tile has read
+      // it): each warp stages 32 columns of its 32 rows, then writes them 4 rows of 128 bytes per
+      // instruction instead of one 16-byte piece of each of 32 rows.
       const size_t slot = ((size_t)(q_start + tok) * p.slot_count + r) * p.num_q_heads + kvh * G + row % G;
-      float* acc = p.ws_acc + slot * kD;
       if (n_mine > 0) {
         tc_fence_after();
-#pragma unroll
+        uint8_t* stage = smem + kOffQ + t * kTileBytes + (warp & 3) * (32 * 128);
+        const int piece = lane & 7;
+#pragma unroll 1
         for (int q4 = 0; q4 < kD / 32; ++q4) {
           uint32_t ov[32];
           tmem_ld32(o_col + 32 * q4, ov);
           tmem_ld_wait();
-          if (row_valid) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<uint4*>(acc + q4 * 32 + i) = make_uint4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+          for (int pc = 0; pc < 8; ++pc)  // 128-byte rows, 16-byte pieces swizzled by the row
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((pc ^ (lane & 7)) << 4)) =
+                make_uint4(ov[4 * pc], ov[4 * pc + 1], ov[4 * pc + 2], ov[4 * pc + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);     // the warp's row this lane copies a piece of
+            const int trow = (warp & 3) * 32 + rr;  // its row in the tile
+            const int rtok = tok0 + t * TOK + trow / G;
+            if (rtok < q_len) {
+              const size_t rslot =
+                  ((size_t)(q_start + rtok) * p.slot_count + r) * p.num_q_heads + kvh * G + trow % G;
+              *reinterpret_cast<uint4*>(p.ws_acc + rslot * kD + q4 * 32 + piece * 4) =
+                  *reinterpret_cast<const uint4*>(stage + rr * 128 + ((piece ^ (rr & 7)) << 4));
+            }
           }
+          __syncwarp();
         }
         if (row_valid) {
           p.ws_ml[slot * 2] = m_run;
